@@ -1,0 +1,406 @@
+/*
+ * zpp_oracle.c -- plain, slow, single-threaded CPU oracle of the ZeRO++
+ * data-parallel codec path (qwZ, qgZ two-hop reduce, sharded mixed-precision
+ * Adam).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call it: only the
+ * tests, the entry point's smoke check and the bench's CPU-baseline leg do.
+ * It shares no code, header, table or helper with the CUDA library.
+ *
+ * Build: gcc -std=c11 -O2 -ffp-contract=off -fno-fast-math -fPIC -shared.
+ * Every floating-point operation below is a separately rounded IEEE fp32
+ * operation (no FMA contraction), in the order written.
+ *
+ * Sources (page title, then section):
+ *  [P1] "Quantized LLM Training at Scale with ZeRO++", section "The Three
+ *       Pillars of ZeRO++": 1 (QWZ, block quantization, 8-bit weights),
+ *       3 (QGZ: one-shot quantization, two-hop all-to-all with reduction,
+ *       tensor slice reordering).
+ *  [P2] "ZeRO-1/2/3 (Zero Redundancy Optimizer)", section "Stage 1" steps
+ *       4-6 (reduce-scatter, fp32 update, write back 16-bit params) and the
+ *       ZeRO++ note (qwZ int8/int4).
+ *  [P3] "ZeRO Stage 2: Gradient Partitioning": reduce-scatter averages, so
+ *       GPU i ends with the averaged gradient of shard i; the optimizer step
+ *       converts the gradient shard to fp32 and updates fp32 master and state.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - qmax = 2^(bits-1) - 1 (127 for int8, 7 for int4; code -8 unused).
+ *  - s = absmax / qmax (fp32 divide); q = clamp(rint(x / s), -qmax, qmax),
+ *    rint = round half to even, fp32 divide per element.
+ *  - s == 0 (all-zero block, or a scale that underflows) -> every code is 0.
+ *  - A tail block covers only the remaining elements; its scale is taken over
+ *    them; no padding codes are written.
+ *  - int4 codes are two's-complement nibbles, element 2i in the low nibble of
+ *    byte i.
+ *  - Dequant: (float)q * s, one rounded multiply; qwZ output bf16 = round to
+ *    nearest even of that.
+ *  - Hop sums: acc = 0; acc = acc + deq(source) for sources in rank order.
+ *  - Slice reorder: slice j = n'G + l' is stored at position p = l'N + n'.
+ *  - Final hop output: g = sum * (1.0f / N_d).  When N == 1, hop 1 is final.
+ *  - Adam: Kingma & Ba with bias correction, eps outside the square root, no
+ *    weight decay.  bc = 1 - beta^t with beta^t by repeated squaring in
+ *    double, rounded to float once; (1 - beta) rounded from double.
+ *  - Master -> 16-bit write-back: bf16 round to nearest even.
+ *  - bits == 32 is an oracle-only identity codec (fp32 payload, no scale) used
+ *    to pin the placement of the reorder and the two hops with exact sums.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_EINVAL 1
+
+/* ---- bf16 <-> fp32 (definitions) -------------------------------------- */
+
+static float bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round to nearest, ties to even, keeping the upper 16 bits of the fp32 word. */
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) /* NaN: keep it a quiet NaN */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lower = u & 0xffffu;
+    uint32_t upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u;
+    return (uint16_t)upper;
+}
+
+/* ---- sizes ------------------------------------------------------------ */
+
+int64_t orc_codes_bytes(int64_t n, int bits)
+{
+    if (bits == 32) return 4 * n;
+    return (n * bits + 7) / 8;
+}
+
+int64_t orc_num_blocks(int64_t n, int64_t block)
+{
+    return (n + block - 1) / block;
+}
+
+static int valid_bits(int bits) { return bits == 4 || bits == 8 || bits == 32; }
+
+/* ---- O1: quantize one block ------------------------------------------- */
+
+static int qmax_of(int bits) { return (1 << (bits - 1)) - 1; }
+
+/* Store code q of element `pos` of a code stream. */
+static void put_code(void* codes, int64_t pos, int bits, int q, float xf)
+{
+    if (bits == 8) {
+        ((int8_t*)codes)[pos] = (int8_t)q;
+    } else if (bits == 4) {
+        uint8_t* b = (uint8_t*)codes + pos / 2;
+        uint8_t nib = (uint8_t)(q & 0xf);
+        if (pos % 2 == 0) *b = (uint8_t)((*b & 0xf0u) | nib);
+        else              *b = (uint8_t)((*b & 0x0fu) | (uint8_t)(nib << 4));
+    } else { /* identity codec */
+        ((float*)codes)[pos] = xf;
+    }
+}
+
+static int get_code(const void* codes, int64_t pos, int bits)
+{
+    if (bits == 8) return ((const int8_t*)codes)[pos];
+    uint8_t b = ((const uint8_t*)codes)[pos / 2];
+    int nib = (pos % 2 == 0) ? (b & 0xf) : (b >> 4);
+    return nib >= 8 ? nib - 16 : nib; /* two's complement nibble */
+}
+
+/* O2: dequantized fp32 value of element `pos`. */
+static float deq(const void* codes, const float* scales, int64_t pos,
+                 int64_t block, int bits)
+{
+    if (bits == 32) return ((const float*)codes)[pos];
+    float s = scales[pos / block];
+    float q = (float)get_code(codes, pos, bits);
+    return q * s;
+}
+
+/* Quantize n fp32 values x[0..n) as one block.  Codes go to element
+ * positions code_pos .. code_pos+n of `codes`; the scale to *scale. */
+static void quant_one_block(const float* x, int64_t n, int bits,
+                            void* codes, int64_t code_pos, float* scale)
+{
+    if (bits == 32) {
+        for (int64_t i = 0; i < n; ++i) put_code(codes, code_pos + i, 32, 0, x[i]);
+        if (scale) *scale = 1.0f;
+        return;
+    }
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    const float qmax = (float)qmax_of(bits);
+    const float s = amax / qmax;
+    *scale = s;
+    for (int64_t i = 0; i < n; ++i) {
+        int q = 0;
+        if (s != 0.0f) {
+            float y = x[i] / s;
+            float r = rintf(y);
+            if (r > qmax) r = qmax;
+            if (r < -qmax) r = -qmax;
+            q = (int)r;
+        }
+        put_code(codes, code_pos + i, bits, q, 0.0f);
+    }
+}
+
+/* Block-quantize a run of n fp32 values in blocks of `block` (tail allowed).
+ * Used for qwZ, for the qgZ one-shot quantization, for the hop-1 requant and,
+ * with block >= n, for global quantization. */
+int orc_block_quant(const float* x, int64_t n, int64_t block, int bits,
+                    void* codes, float* scales)
+{
+    if (n < 0 || block <= 0 || !valid_bits(bits)) return ORC_EINVAL;
+    int64_t nb = orc_num_blocks(n, block);
+    for (int64_t b = 0; b < nb; ++b) {
+        int64_t lo = b * block;
+        int64_t len = (n - lo < block) ? (n - lo) : block;
+        quant_one_block(x + lo, len, bits, codes, lo, scales ? scales + b : NULL);
+    }
+    return ORC_OK;
+}
+
+int orc_block_dequant(const void* codes, const float* scales, int64_t n,
+                      int64_t block, int bits, float* y)
+{
+    if (n < 0 || block <= 0 || !valid_bits(bits)) return ORC_EINVAL;
+    for (int64_t i = 0; i < n; ++i) y[i] = deq(codes, scales, i, block, bits);
+    return ORC_OK;
+}
+
+/* ---- a1/a2: qwZ --------------------------------------------------------- */
+
+/* x_bf16 [nranks][shard] -> codes [nranks][codes_bytes(shard)],
+ * scales [nranks][num_blocks(shard)]; blocks restart at every shard. */
+int orc_qwz_quant(const uint16_t* x, int64_t nranks, int64_t shard, int64_t block,
+                  int bits, void* codes, float* scales)
+{
+    if (nranks < 0 || shard < 0 || block <= 0 || (bits != 4 && bits != 8))
+        return ORC_EINVAL;
+    if (bits == 4 && shard % 2) return ORC_EINVAL;
+    float* tmp = (float*)malloc((size_t)(shard > 0 ? shard : 1) * sizeof(float));
+    if (!tmp) return ORC_EINVAL;
+    int64_t cb = orc_codes_bytes(shard, bits), nb = orc_num_blocks(shard, block);
+    for (int64_t r = 0; r < nranks; ++r) {
+        for (int64_t i = 0; i < shard; ++i) tmp[i] = bf16_to_f32(x[r * shard + i]);
+        orc_block_quant(tmp, shard, block, bits, (uint8_t*)codes + r * cb, scales + r * nb);
+    }
+    free(tmp);
+    return ORC_OK;
+}
+
+/* All-gather receiver: codes/scales of every shard -> the full bf16 tensor. */
+int orc_qwz_dequant(const void* codes, const float* scales, int64_t nranks,
+                    int64_t shard, int64_t block, int bits, uint16_t* y)
+{
+    if (nranks < 0 || shard < 0 || block <= 0 || (bits != 4 && bits != 8))
+        return ORC_EINVAL;
+    if (bits == 4 && shard % 2) return ORC_EINVAL;
+    int64_t cb = orc_codes_bytes(shard, bits), nb = orc_num_blocks(shard, block);
+    for (int64_t r = 0; r < nranks; ++r)
+        for (int64_t i = 0; i < shard; ++i)
+            y[r * shard + i] = orc_f32_to_bf16(
+                deq((const uint8_t*)codes + r * cb, scales + r * nb, i, block, bits));
+    return ORC_OK;
+}
+
+/* ---- a3: slice reorder + one-shot quantization -------------------------- */
+
+/* perm[p] = source slice j stored at message position p.
+ * Slice j = n*G + l belongs to rank (node n, local l); it goes to p = l*N + n,
+ * so that local peer l receives one contiguous chunk of N slots in hop 1 and
+ * node n receives slot n in hop 2. */
+int orc_qgz_slice_perm(int N, int G, int32_t* perm)
+{
+    if (N <= 0 || G <= 0) return ORC_EINVAL;
+    for (int n = 0; n < N; ++n)
+        for (int l = 0; l < G; ++l)
+            perm[l * N + n] = n * G + l;
+    return ORC_OK;
+}
+
+static int qgz_check(int N, int G, int64_t bucket, int64_t block, int bits)
+{
+    if (N <= 0 || G <= 0 || bucket < 0 || block <= 0 || !valid_bits(bits))
+        return ORC_EINVAL;
+    if (bucket % ((int64_t)N * G * block)) return ORC_EINVAL;
+    return ORC_OK;
+}
+
+/* Same as orc_qgz_reorder_quant with an explicit permutation (perm[p] = j). */
+int orc_qgz_reorder_quant_perm(const uint16_t* grads, int N, int G, int64_t bucket,
+                               int64_t block, int bits, const int32_t* perm,
+                               void* codes, float* scales)
+{
+    if (qgz_check(N, G, bucket, block, bits)) return ORC_EINVAL;
+    const int64_t Nd = (int64_t)N * G, L = bucket / Nd;
+    const int64_t cb = orc_codes_bytes(bucket, bits), nb = bucket / block;
+    float* tmp = (float*)malloc((size_t)(L > 0 ? L : 1) * sizeof(float));
+    if (!tmp) return ORC_EINVAL;
+    for (int64_t r = 0; r < Nd; ++r) {
+        uint8_t* rc = (uint8_t*)codes + r * cb;
+        float* rs = scales ? scales + r * nb : NULL;
+        for (int64_t p = 0; p < Nd; ++p) {
+            int64_t j = perm[p];
+            for (int64_t i = 0; i < L; ++i)
+                tmp[i] = bf16_to_f32(grads[r * bucket + j * L + i]);
+            /* blocks of slice j restart at the slice start (L % block == 0) */
+            for (int64_t b = 0; b < L / block; ++b)
+                quant_one_block(tmp + b * block, block, bits, rc, p * L + b * block,
+                                rs ? rs + (p * L + b * block) / block : NULL);
+        }
+    }
+    free(tmp);
+    return ORC_OK;
+}
+
+int orc_qgz_reorder_quant(const uint16_t* grads, int N, int G, int64_t bucket,
+                          int64_t block, int bits, void* codes, float* scales)
+{
+    if (N <= 0 || G <= 0) return ORC_EINVAL;
+    int32_t* perm = (int32_t*)malloc((size_t)N * G * sizeof(int32_t));
+    if (!perm) return ORC_EINVAL;
+    orc_qgz_slice_perm(N, G, perm);
+    int rc = orc_qgz_reorder_quant_perm(grads, N, G, bucket, block, bits, perm,
+                                        codes, scales);
+    free(perm);
+    return rc;
+}
+
+/* ---- a4: hop 1, intra-node dequant -> sum -> requant --------------------- */
+
+/* Destination rank d = n*G + l receives chunk l (N slots of L elements) of
+ * each local peer n*G + g, g = 0..G-1, and sums them in that order.
+ * N > 1: the sum is requantized (same block and bits) into
+ *        codes_out [N_d][codes_bytes(N*L)], scales_out [N_d][N*L/block].
+ * N == 1: hop 1 is the final hop; grad_out[d*L + i] = sum * (1/N_d). */
+int orc_qgz_hop1(const void* codes_in, const float* scales_in, int N, int G,
+                 int64_t bucket, int64_t block, int bits, void* codes_out,
+                 float* scales_out, float* grad_out)
+{
+    if (qgz_check(N, G, bucket, block, bits)) return ORC_EINVAL;
+    const int64_t Nd = (int64_t)N * G, L = bucket / Nd, NL = (int64_t)N * L;
+    const int64_t cb_in = orc_codes_bytes(bucket, bits), nb_in = bucket / block;
+    const int64_t cb_out = orc_codes_bytes(NL, bits), nb_out = NL / block;
+    const float inv_nd = 1.0f / (float)Nd;
+    if (N > 1 && !codes_out) return ORC_EINVAL;
+    if (N == 1 && !grad_out) return ORC_EINVAL;
+    float* acc = (float*)malloc((size_t)(NL > 0 ? NL : 1) * sizeof(float));
+    if (!acc) return ORC_EINVAL;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t l = 0; l < G; ++l) {
+            const int64_t d = n * G + l;
+            for (int64_t e = 0; e < NL; ++e) acc[e] = 0.0f;
+            for (int64_t g = 0; g < G; ++g) {
+                const int64_t src = n * G + g;
+                const uint8_t* c = (const uint8_t*)codes_in + src * cb_in;
+                const float* s = scales_in ? scales_in + src * nb_in : NULL;
+                for (int64_t e = 0; e < NL; ++e)
+                    acc[e] = acc[e] + deq(c, s, l * NL + e, block, bits);
+            }
+            if (N == 1) {
+                for (int64_t e = 0; e < L; ++e) grad_out[d * L + e] = acc[e] * inv_nd;
+            } else {
+                orc_block_quant(acc, NL, block, bits, (uint8_t*)codes_out + d * cb_out,
+                                scales_out ? scales_out + d * nb_out : NULL);
+            }
+        }
+    }
+    free(acc);
+    return ORC_OK;
+}
+
+/* ---- a5: hop 2, inter-node dequant -> sum -> average ---------------------- */
+
+/* Destination rank d = n*G + l receives slot n of rank n'*G + l for
+ * n' = 0..N-1 (hop-1 messages), sums in that order and scales by 1/N_d:
+ * grad_out[d*L + i] is rank d's averaged gradient slice. */
+int orc_qgz_hop2(const void* codes_in, const float* scales_in, int N, int G,
+                 int64_t bucket, int64_t block, int bits, float* grad_out)
+{
+    if (qgz_check(N, G, bucket, block, bits) || N < 2 || !grad_out) return ORC_EINVAL;
+    const int64_t Nd = (int64_t)N * G, L = bucket / Nd, NL = (int64_t)N * L;
+    const int64_t cb_in = orc_codes_bytes(NL, bits), nb_in = NL / block;
+    const float inv_nd = 1.0f / (float)Nd;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t l = 0; l < G; ++l) {
+            const int64_t d = n * G + l;
+            for (int64_t i = 0; i < L; ++i) {
+                float acc = 0.0f;
+                for (int64_t np = 0; np < N; ++np) {
+                    const int64_t src = np * G + l;
+                    acc = acc + deq((const uint8_t*)codes_in + src * cb_in,
+                                    scales_in ? scales_in + src * nb_in : NULL,
+                                    n * L + i, block, bits);
+                }
+                grad_out[d * L + i] = acc * inv_nd;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ---- a6: sharded mixed-precision Adam ----------------------------------- */
+
+static double pow_by_squaring(double b, int64_t t)
+{
+    double r = 1.0;
+    while (t > 0) {
+        if (t & 1) r = r * b;
+        b = b * b;
+        t >>= 1;
+    }
+    return r;
+}
+
+/* Bias corrections and (1 - beta) as the Adam step uses them. */
+void orc_adam_consts(float beta1, float beta2, int32_t t, float* bc1, float* bc2,
+                     float* omb1, float* omb2)
+{
+    *bc1 = (float)(1.0 - pow_by_squaring((double)beta1, t));
+    *bc2 = (float)(1.0 - pow_by_squaring((double)beta2, t));
+    *omb1 = (float)(1.0 - (double)beta1);
+    *omb2 = (float)(1.0 - (double)beta2);
+}
+
+/* One Adam step on n owned parameters with fp32 gradient g:
+ *   m <- b1*m + (1-b1)*g ;  v <- b2*v + (1-b2)*(g*g)
+ *   p <- p - (lr * (m/bc1)) / (sqrt(v/bc2) + eps)
+ *   param_bf16 <- bf16_rne(p)                                              */
+int orc_adam_step(const float* g, int64_t n, float lr, float beta1, float beta2,
+                  float eps, int32_t t, float* master, float* m, float* v,
+                  uint16_t* param)
+{
+    if (n < 0 || t < 1) return ORC_EINVAL;
+    float bc1, bc2, omb1, omb2;
+    orc_adam_consts(beta1, beta2, t, &bc1, &bc2, &omb1, &omb2);
+    for (int64_t i = 0; i < n; ++i) {
+        const float gi = g[i];
+        const float mi = beta1 * m[i] + omb1 * gi;
+        const float vi = beta2 * v[i] + omb2 * (gi * gi);
+        const float mhat = mi / bc1;
+        const float vhat = vi / bc2;
+        const float denom = sqrtf(vhat) + eps;
+        const float p = master[i] - (lr * mhat) / denom;
+        m[i] = mi;
+        v[i] = vi;
+        master[i] = p;
+        if (param) param[i] = orc_f32_to_bf16(p);
+    }
+    return ORC_OK;
+}

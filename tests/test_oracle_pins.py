@@ -1,0 +1,446 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these re-types the oracle's formula: each checks it against a hand
+worked value, a brute-force search, a closed form, an invariant or an
+independent library routine, chosen so that a dropped term, a wrong sign, a
+wrong index or a transposed operand fails at least one of them.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import accounting
+from conftest import golden, golden_rows
+
+RNG = np.random.default_rng(1234)
+
+
+def f32(x):
+    return np.float32(x)
+
+
+# ---- O1: block quantization -----------------------------------------------------
+
+def brute_force_codes(x, s, qmax):
+    """argmin over integers q in [-qmax, qmax] of |fl32(x/s) - q|, ties to even."""
+    out = []
+    for xi in np.asarray(x, dtype=np.float32):
+        if s == 0:
+            out.append(0)
+            continue
+        y = float(np.float32(xi) / np.float32(s))     # IEEE fp32 divide
+        best, bestd = None, None
+        for q in range(-qmax, qmax + 1):
+            d = abs(y - q)
+            if bestd is None or d < bestd or (d == bestd and q % 2 == 0):
+                best, bestd = q, d
+        out.append(best)
+    return np.array(out, dtype=np.int32)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("block", [1, 3, 8, 64])
+def test_codes_brute_force(bits, block):
+    qmax = (1 << (bits - 1)) - 1
+    for trial in range(30):
+        n = int(RNG.integers(1, 3 * block + 2))
+        scale = float(10.0 ** RNG.uniform(-6, 2))
+        x = (RNG.standard_normal(n) * scale).astype(np.float32)
+        if trial % 3 == 0:            # bf16-valued inputs, as the path sees them
+            x = (x.view(np.uint32) & 0xFFFF0000).view(np.float32)
+        codes, scales = oracle.block_quant(x, block, bits)
+        q = oracle.unpack_codes(codes, n, bits)
+        for b in range(scales.size):
+            blk = x[b * block:(b + 1) * block]
+            amax = float(np.max(np.abs(blk)))
+            # scale: correctly rounded fp32 of absmax/qmax (double then round
+            # is correct rounding for a quotient of fp32 values)
+            assert scales[b] == np.float32(amax / qmax)
+            assert np.array_equal(q[b * block:(b + 1) * block],
+                                  brute_force_codes(blk, scales[b], qmax))
+
+
+def test_round_half_even_ties_worked_by_hand():
+    rows = golden_rows("quant_ties.txt")
+    x = np.array([float(r[0]) for r in rows], dtype=np.float32)
+    want = np.array([int(r[1]) for r in rows])
+    codes, scales = oracle.block_quant(x, x.size, 8)
+    assert scales[0] == 1.0
+    assert np.array_equal(oracle.unpack_codes(codes, x.size, 8), want)
+
+
+def test_int4_packing_worked_by_hand():
+    x = np.array([7, -7, 1, -1, 0, 3, -4, 5], dtype=np.float32)
+    codes, scales = oracle.block_quant(x, 8, 4)
+    assert scales[0] == 1.0
+    want = {int(r[0]): int(r[1], 16) for r in golden_rows("int4_packing.txt")}
+    assert [int(b) for b in codes] == [want[i] for i in range(4)]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_dequant_error_within_half_scale(bits):
+    qmax = (1 << (bits - 1)) - 1
+    u = 2.0 ** -24
+    for _ in range(20):
+        n, block = 4096, int(RNG.choice([64, 256, 1000]))
+        x = (RNG.standard_t(3, n) * 1e-3).astype(np.float32)
+        codes, scales = oracle.block_quant(x, block, bits)
+        y = oracle.block_dequant(codes, scales, n, block, bits).astype(np.float64)
+        s = np.repeat(scales.astype(np.float64), block)[:n]
+        # |fl(q s) - x| <= s/2 + u(|x| + |q s|) <= s/2 + 2u (qmax+1) s
+        bound = s / 2 + 2 * u * (qmax + 1) * s
+        assert np.all(np.abs(y - x.astype(np.float64)) <= bound)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_special_blocks(bits):
+    qmax = (1 << (bits - 1)) - 1
+    # absmax element -> +-qmax
+    x = np.array([0.1, -0.3, 0.25, 0.05], dtype=np.float32)
+    c, s = oracle.block_quant(x, 4, bits)
+    assert oracle.unpack_codes(c, 4, bits)[1] == -qmax
+    # zero block -> scale 0, codes 0
+    c, s = oracle.block_quant(np.zeros(6, np.float32), 6, bits)
+    assert s[0] == 0 and not oracle.unpack_codes(c, 6, bits).any()
+    # one nonzero value -> +-qmax, the rest 0
+    x = np.zeros(8, np.float32)
+    x[5] = -3e-7
+    c, s = oracle.block_quant(x, 8, bits)
+    q = oracle.unpack_codes(c, 8, bits)
+    assert q[5] == -qmax and np.count_nonzero(q) == 1
+    # tail block: scale over the remaining elements only
+    x = np.concatenate([np.full(8, 100.0, np.float32), np.array([1.0, -2.0], np.float32)])
+    c, s = oracle.block_quant(x, 8, bits)
+    assert s.size == 2 and s[1] == np.float32(2.0 / qmax)
+    assert oracle.unpack_codes(c, 10, bits)[9] == -qmax
+    assert np.array_equal(oracle.unpack_codes(c, 10, bits)[8:],
+                          brute_force_codes(x[8:], s[1], qmax))
+
+
+def test_subnormal_scale_is_honoured():
+    # absmax tiny enough that s = absmax/127 is an fp32 subnormal
+    x = np.array([2.0 ** -130, -2.0 ** -131, 2.0 ** -133], dtype=np.float32)
+    c, s = oracle.block_quant(x, 3, 8)
+    assert 0 < s[0] < np.finfo(np.float32).tiny
+    assert np.array_equal(oracle.unpack_codes(c, 3, 8), brute_force_codes(x, s[0], 127))
+
+
+def test_bf16_round_to_nearest_even_matches_torch():
+    vals = np.concatenate([
+        RNG.standard_normal(20000).astype(np.float32) * 10.0 ** RNG.uniform(-30, 30, 20000),
+        # exact ties between two bf16 neighbours, both parities
+        ((np.arange(1000, dtype=np.uint32) << 16) | 0x8000).view(np.float32) + 0,
+        np.array([0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, 1e-40, -1e-40], np.float32),
+    ]).astype(np.float32)
+    vals = vals[np.isfinite(vals)]
+    ours = oracle.f32_to_bf16(vals)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ---- a1/a2: qwZ shards ------------------------------------------------------------
+
+def test_qwz_blocks_restart_at_every_shard():
+    shard, block = 300, 256
+    x = np.ones(2 * shard, np.float32)
+    x[shard - 1] = 127.0                 # large value at the end of shard 0
+    x[shard:] = 2.0                      # shard 1 is small
+    xb = oracle.f32_to_bf16(x)
+    codes, scales = oracle.qwz_quant(xb, 2, shard, block, 8)
+    assert scales.size == 4
+    assert scales[1] == 1.0                             # shard 0 tail block sees 127
+    assert scales[2] == np.float32(2.0 / 127.0)         # shard 1 first block does not
+    q = oracle.unpack_codes(codes, 2 * shard, 8)
+    assert np.all(q[shard:] == 127)
+    y = oracle.qwz_dequant(codes, scales, 2, shard, block, 8)
+    assert y[shard - 1] == oracle.f32_to_bf16([127.0])[0]
+
+
+def test_qwz_dequant_bound_and_bf16_rounding():
+    nranks, shard, block = 3, 1000, 128
+    w = (RNG.standard_normal(nranks * shard) * 0.02).astype(np.float32)
+    wb = oracle.f32_to_bf16(w)
+    xf = oracle.bf16_bits_to_f32(wb).astype(np.float64)
+    for bits in (8, 4):
+        qmax = (1 << (bits - 1)) - 1
+        codes, scales = oracle.qwz_quant(wb, nranks, shard, block, bits)
+        y = oracle.bf16_bits_to_f32(oracle.qwz_dequant(codes, scales, nranks, shard, block, bits))
+        nb = -(-shard // block)
+        s = np.concatenate([np.repeat(scales[r * nb:(r + 1) * nb].astype(np.float64), block)[:shard]
+                            for r in range(nranks)])
+        # s/2 from the code plus half a bf16 ulp (2^-8 relative) from the output rounding
+        bound = s / 2 + 2 * 2.0 ** -24 * (qmax + 1) * s + np.abs(y) * 2.0 ** -8
+        assert np.all(np.abs(y.astype(np.float64) - xf) <= bound)
+
+
+# ---- O4: slice reordering ------------------------------------------------------------
+
+def test_slice_perm_worked_example_and_identities():
+    # N=2 nodes, G=3: position p = l*N + n holds slice j = n*G + l
+    assert list(oracle.qgz_slice_perm(2, 3)) == [0, 3, 1, 4, 2, 5]
+    for k in range(1, 9):
+        assert list(oracle.qgz_slice_perm(1, k)) == list(range(k))
+        assert list(oracle.qgz_slice_perm(k, 1)) == list(range(k))
+    for N in range(1, 6):
+        for G in range(1, 6):
+            assert sorted(oracle.qgz_slice_perm(N, G)) == list(range(N * G))
+
+
+def direct_reduce_scatter(grads_f64, Nd, bucket):
+    """Textbook reduce-scatter with averaging: rank r gets the mean over ranks of
+    slice r ("ZeRO Stage 2: Gradient Partitioning", Reduce-Scatter step 2)."""
+    L = bucket // Nd
+    g = grads_f64.reshape(Nd, Nd, L)
+    return g.sum(axis=0)  # [slice r][i]; divided by Nd by the caller
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4])
+@pytest.mark.parametrize("G", [1, 2, 3, 4])
+def test_two_hop_placement_equals_reduce_scatter(N, G):
+    """Identity codec + small-integer inputs: every sum is exact, so the two-hop
+    chain must reproduce the direct reduce-scatter exactly."""
+    Nd, L = N * G, 16
+    bucket = Nd * L
+    vals = RNG.integers(-50, 51, size=Nd * bucket).astype(np.float32)
+    gb = oracle.f32_to_bf16(vals)
+    got = oracle.qgz_reduce_scatter(gb, N, G, bucket, L, 32)
+    sums = direct_reduce_scatter(vals.astype(np.float64), Nd, bucket)
+    inv = np.float32(1.0) / np.float32(Nd)
+    want = (sums.astype(np.float32) * inv).reshape(-1)
+    assert np.array_equal(got, want)
+    if Nd & (Nd - 1) == 0:   # power of two: the average itself is exact
+        assert np.array_equal(got.astype(np.float64), (sums / Nd).reshape(-1))
+
+
+@pytest.mark.parametrize("N,G", [(2, 2), (2, 3), (3, 2), (4, 4)])
+def test_without_reorder_slices_are_misplaced(N, G):
+    Nd, L = N * G, 8
+    bucket = Nd * L
+    vals = RNG.integers(-50, 51, size=Nd * bucket).astype(np.float32)
+    gb = oracle.f32_to_bf16(vals)
+    codes, scales = oracle.qgz_reorder_quant(gb, N, G, bucket, L, 32,
+                                             perm=np.arange(Nd, dtype=np.int32))
+    c1, s1 = oracle.qgz_hop1(codes, scales, N, G, bucket, L, 32)
+    got = oracle.qgz_hop2(c1, s1, N, G, bucket, L, 32)
+    want = (direct_reduce_scatter(vals.astype(np.float64), Nd, bucket).astype(np.float32)
+            * (np.float32(1) / np.float32(Nd))).reshape(-1)
+    wrong = [r for r in range(Nd) if not np.array_equal(got[r * L:(r + 1) * L], want[r * L:(r + 1) * L])]
+    assert wrong, "without the reorder some rank must receive another rank's slice"
+
+
+def test_hop_sum_is_in_rank_order():
+    """fp32: (0 + 2^24) + 1 = 2^24 (ties to even), then - 2^24 = 0; any other
+    order of the three terms gives 1 or 2^24 + ... so only rank order gives 0."""
+    N, G, L = 1, 3, 4
+    Nd, bucket = 3, 12
+    vals = np.zeros((Nd, bucket), np.float32)
+    vals[0, :] = 2.0 ** 24
+    vals[1, :] = 1.0
+    vals[2, :] = -(2.0 ** 24)
+    got = oracle.qgz_reduce_scatter(oracle.f32_to_bf16(vals.reshape(-1)), N, G, bucket, L, 32)
+    assert np.all(got == 0.0)
+    vals[[0, 1]] = vals[[1, 0]]          # 1 first: (1 + 2^24) = 2^24 ... also 0
+    got = oracle.qgz_reduce_scatter(oracle.f32_to_bf16(vals.reshape(-1)), N, G, bucket, L, 32)
+    assert np.all(got == 0.0)
+    vals[[1, 2]] = vals[[2, 1]]          # 2^24 - 2^24 + 1 = 1
+    got = oracle.qgz_reduce_scatter(oracle.f32_to_bf16(vals.reshape(-1)), N, G, bucket, L, 32)
+    assert np.all(got == np.float32(1.0) * (np.float32(1) / np.float32(3)))
+
+
+# ---- O3-O5 with the real codecs --------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("N,G", [(1, 4), (2, 2), (2, 4), (4, 2)])
+def test_identical_exact_gradients_average_to_themselves(bits, N, G):
+    """Every rank holds the same bucket, each block exactly q*s0 with s0 a power
+    of two and one element at +-qmax: hop-1 requant and both averages are exact,
+    so the reduce-scatter returns each rank's own slice unchanged."""
+    qmax = (1 << (bits - 1)) - 1
+    Nd, block = N * G, 64
+    L = 2 * block
+    bucket = Nd * L
+    s0 = 2.0 ** -12
+    q = RNG.integers(-qmax, qmax + 1, size=bucket)
+    q[::block] = qmax * RNG.choice([-1, 1], size=bucket // block)
+    x = (q * s0).astype(np.float32)
+    gb = oracle.f32_to_bf16(np.tile(x, Nd))
+    got = oracle.qgz_reduce_scatter(gb, N, G, bucket, block, bits)
+    assert np.array_equal(got, x)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("N,G", [(1, 8), (2, 2), (2, 4), (3, 2), (4, 4)])
+def test_reduce_scatter_error_bound(bits, N, G):
+    Nd, block = N * G, 64
+    L = 3 * block
+    bucket = Nd * L
+    x = (RNG.standard_normal(Nd * bucket) * 1e-3).astype(np.float32)
+    gb = oracle.f32_to_bf16(x)
+    xf = oracle.bf16_bits_to_f32(gb).astype(np.float64).reshape(Nd, Nd, L)   # [rank][slice][i]
+    exact = xf.sum(axis=0) / Nd                                              # [slice r][i]
+    codes, scales = oracle.qgz_reorder_quant(gb, N, G, bucket, block, bits)
+    sc = scales.reshape(Nd, bucket // block).astype(np.float64)
+    perm = oracle.qgz_slice_perm(N, G)
+    pos = np.argsort(perm)                       # slice j -> position
+    # per-element bound: half a scale for every quantization the value went through
+    e1 = np.zeros((Nd, L))
+    for r in range(Nd):
+        for j in range(Nd):
+            p = pos[j]
+            e1[j] += np.repeat(sc[r, p * L // block:(p + 1) * L // block], block) / 2
+    if N == 1:
+        got = oracle.qgz_hop1(codes, scales, N, G, bucket, block, bits)
+        e2 = np.zeros((Nd, L))
+    else:
+        c1, s1 = oracle.qgz_hop1(codes, scales, N, G, bucket, block, bits)
+        got = oracle.qgz_hop2(c1, s1, N, G, bucket, block, bits)
+        s1 = s1.reshape(Nd, N * L // block).astype(np.float64)
+        e2 = np.zeros((Nd, L))
+        for n in range(N):
+            for l in range(G):
+                d = n * G + l
+                for n2 in range(N):
+                    src = n2 * G + l
+                    e2[d] += np.repeat(s1[src, n * L // block:(n + 1) * L // block], block) / 2
+    qmax = (1 << (bits - 1)) - 1
+    slack = (2 * Nd + 4) * 2.0 ** -23 * (np.abs(xf).sum(axis=0) + e1 + e2 + 1e-30) \
+        + 2 * 2.0 ** -24 * (qmax + 1) * (e1 + e2)
+    bound = (e1 + e2) / Nd + slack
+    err = np.abs(got.reshape(Nd, L).astype(np.float64) - exact)
+    assert np.all(err <= bound)
+
+
+# ---- O6: Adam ---------------------------------------------------------------------------
+
+def test_adam_first_step_closed_form():
+    n = 5000
+    g = (RNG.standard_normal(n) * 1e-3).astype(np.float32)
+    g[:10] = 0.0
+    p0 = (RNG.standard_normal(n) * 0.02).astype(np.float32)
+    lr, b1, b2, eps = 1e-4, 0.9, 0.999, 1e-8
+    z = np.zeros(n, np.float32)
+    p, m, v, pb = oracle.adam_step(g, p0, z, z, lr, b1, b2, eps, 1)
+    b1f, b2f = np.float64(np.float32(b1)), np.float64(np.float32(b2))
+    gd = g.astype(np.float64)
+    # m' = (1 - b1) g, v' = (1 - b2) g^2 (each within a couple of roundings)
+    assert np.allclose(m, (1 - b1f) * gd, rtol=3e-7, atol=0)
+    assert np.allclose(v, (1 - b2f) * gd * gd, rtol=5e-7, atol=0)
+    # bias corrections cancel: p' = p - lr g / (|g| + eps)
+    want = p0.astype(np.float64) - lr * gd / (np.abs(gd) + eps)
+    # the update term lr*g/(|g|+eps) carries a few fp32 roundings (relative
+    # 2^-24 each) and the result one more
+    ulp = np.spacing(np.abs(want).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(p - want) <= 2 * ulp + 8 * 2.0 ** -24 * lr)
+    assert np.all(p[:10] == p0[:10])               # zero gradient: no move
+    # the 16-bit write-back is the rounded master
+    assert np.array_equal(pb, oracle.f32_to_bf16(p))
+
+
+def test_adam_later_steps_against_double():
+    """Each step against a float64 recomputation of the textbook update from
+    the same fp32 state; error bounded by a few roundings of each term."""
+    n = 3000
+    u = 2.0 ** -24
+    lr, b1, b2, eps = 3e-4, 0.9, 0.95, 1e-6
+    p = (RNG.standard_normal(n) * 0.02).astype(np.float32)
+    m = (RNG.standard_normal(n) * 1e-4).astype(np.float32)
+    v = np.abs(RNG.standard_normal(n) * 1e-6).astype(np.float32)
+    b1f, b2f = float(np.float32(b1)), float(np.float32(b2))
+    for t in (2, 3, 10, 1000):
+        g = (RNG.standard_normal(n) * 1e-3).astype(np.float32)
+        pd, md, vd, gd = (a.astype(np.float64) for a in (p, m, v, g))
+        p, m, v, _ = oracle.adam_step(g, p, m, v, lr, b1, b2, eps, t)
+        mw = b1f * md + (1 - b1f) * gd
+        vw = b2f * vd + (1 - b2f) * gd * gd
+        mh, vh = mw / (1 - b1f ** t), vw / (1 - b2f ** t)
+        upd = lr * mh / (np.sqrt(vh) + eps)
+        pw = pd - upd
+        assert np.all(np.abs(m - mw) <= 3 * u * (b1f * np.abs(md) + (1 - b1f) * np.abs(gd)) + 1e-45)
+        assert np.all(np.abs(v - vw) <= 4 * u * (b2f * vd + (1 - b2f) * gd * gd) + 1e-45)
+        assert np.all(np.abs(p - pw) <= u * np.abs(pw) + 12 * u * np.abs(upd) + 1e-45)
+        # and the whole trajectory stays a 1e-5-relative match of the textbook values
+        assert np.allclose(m, mw, rtol=1e-5, atol=1e-5 * np.abs(gd).max())
+
+
+def test_adam_bias_constants():
+    bc1, bc2, o1, o2 = oracle.adam_consts(0.9, 0.999, 1)
+    assert bc1 == np.float32(1 - np.float64(np.float32(0.9)))
+    assert o1 == bc1 and o2 == bc2
+    bc1, bc2, _, _ = oracle.adam_consts(0.9, 0.999, 7)
+    assert bc1 == np.float32(1 - np.float64(np.float32(0.9)) ** 7)
+    assert bc2 == np.float32(1 - np.float64(np.float32(0.999)) ** 7)
+
+
+# ---- O7: accounting ----------------------------------------------------------------------
+
+def test_message_sizes_match_oracle_arrays():
+    n, block = 10_000, 256
+    x = (RNG.standard_normal(n) * 0.02).astype(np.float32)
+    for bits in (8, 4):
+        c, s = oracle.block_quant(x, block, bits)
+        assert c.nbytes + s.nbytes == accounting.quantized_bytes(n, block, bits)
+
+
+def test_volume_fractions_match_pages():
+    gv = golden("zeropp_volume.txt")
+    z3 = accounting.zero3_volume()
+    assert z3["fwd"] == Fraction(gv["zero3_fwd_allgather_M"])
+    assert z3["bwd"] == Fraction(gv["zero3_bwd_allgather_M"])
+    assert z3["grad"] == Fraction(gv["zero3_reduce_scatter_M"])
+    assert z3["total"] == Fraction(gv["zero3_total_M"])
+    phi = 7 * 10 ** 9
+    for B in (64, 256, 512, 2048, 4096):
+        v = accounting.zeropp_volume(phi - phi % B, B, 8, B, 4)
+        # codes exactly the printed fractions, plus 4 B of scale per B elements
+        assert v["fwd"] == Fraction(gv["qwz_fwd_M"]) + Fraction(2, B)
+        assert v["grad"] == Fraction(gv["qgz_grad_M"]) + Fraction(2, B)
+        assert v["bwd"] == Fraction(gv["hpz_bwd_cross_node_M"])
+        assert v["total"] == Fraction(gv["zeropp_total_M"]) + Fraction(4, B)
+        assert z3["total"] / v["total"] < 4 and abs(z3["total"] / v["total"] - 4) < 100 / B
+    assert Fraction(gv["stage3_per_gpu_phi"]) / Fraction(gv["dp_per_gpu_phi"]) == \
+        Fraction(gv["stage3_vs_dp_ratio"])
+
+
+def test_memory_formulas_match_pages():
+    gm = golden("zero_memory.txt")
+    GB = 10 ** 9
+    assert accounting.rank_memory(0, 175 * GB, 64) == int(gm["dp_175B_GB"]) * GB
+    assert accounting.rank_memory(0, 7 * GB, 64) == int(gm["dp_7B_GB"]) * GB
+    assert accounting.rank_memory(0, 1, 1) == int(gm["bytes_per_param_dp"])
+    for nd in (1, 2, 8, 64, 1000):
+        phi = 7 * GB
+        assert accounting.rank_memory(1, phi, nd) == 4 * phi + Fraction(12 * phi, nd)
+        assert accounting.rank_memory(2, phi, nd) == 2 * phi + Fraction(14 * phi, nd)
+        assert accounting.rank_memory(3, phi, nd) == Fraction(16 * phi, nd)
+    s2 = accounting.rank_memory(2, 7 * GB, 64)
+    assert s2 == Fraction(gm["stage2_7B_nd64_formula_GB"]) * GB
+    # the page's "14 GB of parameters" is the full 16-bit replica
+    assert accounting.rank_buffers(2, 7 * GB, 64)[0].nbytes == int(gm["stage2_7B_nd64_params_GB"]) * GB
+    # the page's printed total (14.9 GB) disagrees with its own formula
+    assert s2 != Fraction(gm["stage2_7B_nd64_page_total_GB"]) * GB
+    assert accounting.rank_memory(3, 7 * GB, 64) == Fraction(175, 100) * GB
+
+
+def test_two_hop_avoids_cross_node_blow_up():
+    for N, G in ((2, 8), (8, 8), (16, 8), (4, 2)):
+        c = accounting.cross_node_bytes(N, G, N * G * 4096, 256, 4)
+        assert c["flat"] == G * c["two_hop"]
+    c = accounting.cross_node_bytes(1, 8, 8 * 4096, 256, 4)
+    assert c["two_hop"] == 0 and c["flat"] == 0
+
+
+# ---- O8: block vs global quantization ------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_block_quantization_beats_global(bits):
+    import synth
+    from synth import workloads as W
+    for recipe in (W.WEIGHT_RECIPE, W.GRAD_NORMAL, W.GRAD_T3_OUTLIERS):
+        x = synth.fill(recipe, 0, synth.WEIGHTS, 0, 1 << 16).float().numpy()
+        e = accounting.quant_errors(x, 256, bits)
+        assert e["block"]["rmse"] <= e["global"]["rmse"]
+        assert e["rmse_ratio"] > 1.0
