@@ -216,6 +216,24 @@ def test_two_hop_placement_equals_reduce_scatter(N, G):
         assert np.array_equal(got.astype(np.float64), (sums / Nd).reshape(-1))
 
 
+@pytest.mark.parametrize("N,G", [(2, 2), (2, 3), (3, 2), (3, 4)])
+def test_hop1_message_is_the_node_local_partial_sum(N, G):
+    """Identity codec: after the intra-node all-to-all and reduction, rank
+    (n, l) holds, in slot k, the sum over the G ranks of node n (ranks n*G..n*G+G-1)
+    of slice k*G + l -- the part of rank (k, l)'s slice that node n contributes."""
+    Nd, L = N * G, 8
+    bucket = Nd * L
+    vals = RNG.integers(-50, 51, size=Nd * bucket).astype(np.float32)
+    codes, scales = oracle.qgz_reorder_quant(oracle.f32_to_bf16(vals), N, G, bucket, L, 32)
+    c1, _ = oracle.qgz_hop1(codes, scales, N, G, bucket, L, 32)
+    x = vals.reshape(N, G, Nd, L)            # [node][local][slice][i]
+    c1 = c1.reshape(N, G, N, L)              # [node][local][slot][i]
+    for n in range(N):
+        for l in range(G):
+            for k in range(N):
+                assert np.array_equal(c1[n, l, k], x[n, :, k * G + l].sum(axis=0))
+
+
 @pytest.mark.parametrize("N,G", [(2, 2), (2, 3), (3, 2), (4, 4)])
 def test_without_reorder_slices_are_misplaced(N, G):
     Nd, L = N * G, 8
