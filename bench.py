@@ -1,0 +1,529 @@
+#!/usr/bin/env python
+"""Throughput of the ZeRO++ data-parallel codec path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input
+with every simulated rank's buffers resident in HBM:
+
+    qwZ quant (all ranks' weight shards) -> qwZ dequant (the all-gather
+    receiver) -> qgZ reorder + one-shot quant (all ranks' buckets) -> hop 1
+    [-> hop 2] -> x 1/N_d fused into the sharded Adam step.
+
+Default workload: the llama-layer bucket (Phi = 202,375,168 bf16 parameters,
+N_d = 8 simulated as 1 node x 8 GPUs, qwZ int8 B=512, qgZ int4 B=512, Adam on
+all 8 owned shards).  `value` is algorithmic bytes moved per step (the bytes
+each kernel must read and write, summed over the pass) divided by the step
+time, in GB/s; `qgz_bucket_elems_per_s` is N_d * bucket / (qgZ kernels' time).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+    python bench.py --impl reference ...      # the CPU oracle, same metric
+
+Multi-GPU (torchrun, one process per GPU): every rank runs an independent
+replica of the whole simulated job (the path has no real collective on one
+device); `value` = bytes of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "codec+Adam GB/s and % of GB300 HBM peak; qgZ bucket elements/s at N_d"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+KERNEL_OF = {  # launch name -> CUDA kernel (for the roofline and the ncu summaries)
+    "qwz_quant": "quant_kernel<BITS, false>",
+    "qwz_dequant": "dequant_kernel<BITS>",
+    "qgz_reorder_quant": "quant_kernel<BITS, true>",
+    "qgz_hop1": "hop_kernel<BITS, 0>",
+    "qgz_final_hop": "hop_kernel<BITS, 1>",
+}
+KERNEL_SRC = {"qwz_quant": "quant.cu", "qwz_dequant": "quant.cu", "qgz_reorder_quant": "quant.cu",
+              "qgz_hop1": "hop.cu", "qgz_final_hop": "hop.cu"}
+
+
+# ---- workload -> algorithmic bytes ------------------------------------------------
+
+def codes_bytes(n, bits):
+    return (n * bits + 7) // 8
+
+
+def msg_bytes(n, block, bits):
+    return codes_bytes(n, bits) + 4 * (-(-n // block))
+
+
+def launch_bytes(wl):
+    """[(launch name, algorithmic bytes)] of one pass, in launch order."""
+    out = []
+    q, g = wl.qwz, wl.qgz
+    if q is not None:
+        shards = [q.shard] * q.calls
+        if q.tail_shard:
+            shards[-1] = q.tail_shard
+        for s in shards:
+            m = q.nranks * msg_bytes(s, q.block, q.bits)
+            out.append(("qwz_quant", 2 * q.nranks * s + m))
+            out.append(("qwz_dequant", m + 2 * q.nranks * s))
+    if g is not None:
+        nd, b = g.nd, g.bucket
+        m1 = nd * msg_bytes(b, g.block, g.bits)
+        out.append(("qgz_reorder_quant", 2 * nd * b + m1))
+        final_extra = (26 * b) if wl.fused_adam else 4 * b
+        if g.nodes == 1:
+            out.append(("qgz_final_hop", m1 + final_extra))
+        else:
+            m2 = nd * msg_bytes(g.nodes * g.slice_elems, g.block, g.bits)
+            out.append(("qgz_hop1", m1 + m2))
+            out.append(("qgz_final_hop", m2 + final_extra))
+    return out
+
+
+def workload_config(wl, name):
+    q, g = wl.qwz, wl.qgz
+    cfg = {"workload": wl.name, "name": name}
+    if q is not None:
+        cfg.update(qwz_phi=q.phi, qwz=f"int{q.bits} B={q.block}", qwz_nranks=q.nranks,
+                   qwz_calls=q.calls)
+    if g is not None:
+        cfg.update(N_d=g.nd, topology=f"{g.nodes}x{g.gpus_per_node}", bucket_per_rank=g.bucket,
+                   qgz=f"int{g.bits} B={g.block}", adam="fused on the final hop" if wl.fused_adam
+                   else "none")
+    per_step = sum(b for _, b in launch_bytes(wl))
+    if per_step > 4 * L2_BYTES:
+        cfg["l2"] = (f"inputs larger than L2: {per_step / 1e9:.2f} GB moved per step vs "
+                     f"{L2_BYTES / 2**20:.0f} MiB L2; no flush")
+    else:
+        cfg["l2"] = (f"L2-resident: {per_step / 1e6:.1f} MB moved per step fits the "
+                     f"{L2_BYTES / 2**20:.0f} MiB L2; not a roofline configuration")
+    cfg["arithmetic"] = "bf16 in, int8/int4 codes + fp32 scales, fp32 sums and Adam"
+    return cfg
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_table():
+    """ncu DRAM bytes per launch recorded in profiles/traffic.txt, keyed by
+    launch name, workload name and the sha1 of the kernel's source file; a
+    row whose source hash no longer matches is ignored (null traffic)."""
+    import hashlib
+    rows = {}
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return rows
+    for line in open(p):
+        line = line.split("#", 1)[0].split()
+        if len(line) >= 4:
+            name, wname, sha, byts = line[:4]
+            rows[(name, wname)] = (sha, float(byts))
+    cur = {}
+    for name, src in KERNEL_SRC.items():
+        path = os.path.join(ROOT, "gradient_comm_codecs_gb300", "csrc", src)
+        h = hashlib.sha1(open(path, "rb").read())
+        h.update(open(os.path.join(ROOT, "gradient_comm_codecs_gb300", "csrc",
+                                   "zpp_device.cuh"), "rb").read())
+        cur[name] = h.hexdigest()[:12]
+    return {k: v[1] for k, v in rows.items() if cur.get(k[0]) == v[0]}
+
+
+# ---- clocks --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", device_id], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if len(inside) < 2:
+            inside = [p for t, p in self.samples if t0 - 0.5 <= t <= t1 + 0.5]
+            note = "timed region shorter than the sampling period: samples within 0.5 s of it"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        pw = [num(p[3]) for p in inside if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in inside for n, v in zip(names, p[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+# ---- the GPU arm ------------------------------------------------------------------------
+
+def fill_inputs(path, wl):
+    import torch
+    import synth
+    from synth import workloads as W
+    chunk = 1 << 27
+    if wl.qwz is not None:
+        synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, path.qwz.phi, out=path.w, chunk=chunk)
+    if wl.qgz is not None:
+        g = wl.qgz
+        for r in range(g.nd):
+            synth.fill(g.grad, wl.seed, synth.grad_stream(r), 0, g.bucket,
+                       out=path.grads[r * g.bucket:(r + 1) * g.bucket], chunk=chunk)
+        if path.adam is not None:
+            synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, g.bucket, out=path.param,
+                       chunk=chunk)
+            path.master.copy_(path.param.float())
+    torch.cuda.synchronize()
+
+
+def run_gpu(args, wl, rank, world, device):
+    import torch
+    import gradient_comm_codecs_gb300 as Z
+    from gradient_comm_codecs_gb300 import _build
+    _build.build()
+
+    q, g = wl.qwz, wl.qgz
+    qs = Z.QwzSpec(q.nranks, q.shard, q.block, q.bits, chunks=q.calls,
+                   tail_shard=q.tail_shard) if q else None
+    gs = Z.QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits) if g else None
+    a = wl.adam
+    adam = Z.AdamSpec(a.lr, a.beta1, a.beta2, a.eps, a.step) if (g and wl.fused_adam) else None
+    path = Z.CodecPath(qs, gs, adam, device=device, keep_grad=False)
+    fill_inputs(path, wl)
+    stream = torch.cuda.current_stream(device)
+    lb = launch_bytes(wl)
+    step_bytes = sum(b for _, b in lb)
+
+    def one_step(i, events=None):
+        mark = None
+        if events is not None:
+            def mark(name):
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(stream)
+                events.append((name, ev))
+        path.run(stream, adam_step=1 + i, mark=mark)
+
+    for i in range(args.warmup):
+        one_step(i)
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(device)
+    dev_id = str(getattr(props, "uuid", "")) or str(device.index)
+    if dev_id and not dev_id.startswith("GPU-") and "-" in dev_id:
+        dev_id = "GPU-" + dev_id
+    sampler = ClockSampler(dev_id)
+    time.sleep(0.3)
+
+    events = []
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        events.append(("__step__", None))
+        one_step(args.warmup + i, events)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+
+    total_ms = start.elapsed_time(end)
+    # per-launch durations from consecutive events
+    per = {}
+    prev = start
+    for name, ev in events:
+        if name == "__step__":
+            continue
+        per.setdefault(name, []).append(prev.elapsed_time(ev))
+        prev = ev
+    ms_step = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    peak, peak_kind = measured_peak()
+    kernels = {}
+    bytes_of = {}
+    for name, b in lb:
+        bytes_of.setdefault(name, []).append(b)
+    for name, ts in per.items():
+        nb = sum(bytes_of[name]) / len(bytes_of[name])
+        avg = sum(ts) / len(ts)
+        kernels[name] = {"kernel": KERNEL_OF[name], "launches": len(ts), "avg_ms": avg,
+                         "bytes_per_launch": nb, "gbs": nb / (avg * 1e-3) / 1e9,
+                         "frac_of_peak": nb / (avg * 1e-3) / 1e9 / peak,
+                         "share": sum(ts) / total_ms}
+    dom = max(kernels, key=lambda k: kernels[k]["share"])
+    traffic = traffic_table().get((dom, args.config))
+    dk = kernels[dom]
+    roofline = {"bound": "hbm", "kernel": dk["kernel"], "launch": dom,
+                "achieved": dk["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": dk["gbs"] / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "traffic": traffic, "algorithmic_bytes": dk["bytes_per_launch"]}
+
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    qgz_ms = sum(sum(per[n]) for n in per if n.startswith("qgz")) / args.steps
+    qgz_eps = (g.nd * g.bucket / (qgz_ms * 1e-3)) if g else None
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, path, wl, stream, step_bytes, world, device)
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic: seeded counter-based generator (lowbias32 hash -> "
+        "2^20-entry quantile table), weights N(0,0.02), grads per the workload",
+        "config": workload_config(wl, args.config),
+        "pct_hbm_peak_measured": 100.0 * value / world / peak,
+        "pct_hbm_peak_nominal": 100.0 * value / world / NOMINAL_HBM_GBS,
+        "qgz_bucket_elems_per_s": qgz_eps * world if qgz_eps else None,
+        "bytes_per_step": step_bytes,
+        "gpu_launches": sum(len(v) for v in per.values()),
+        "kernels": kernels, "roofline": roofline, "clocks": clocks, "e2e": e2e,
+        "impl": "ours",
+    }
+    del path
+    return res
+
+
+def run_e2e(args, path, wl, stream, step_bytes, world, device):
+    import torch
+    steps = max(3, min(args.steps, 30))
+    w_host = path.w.cpu().pin_memory() if path.qwz is not None else None
+    g_host = path.grads.cpu().pin_memory() if path.qgz is not None else None
+    p_host = None
+    if path.qgz is not None and path.adam is not None:
+        p_host = torch.empty(path.qgz.bucket, dtype=torch.bfloat16).pin_memory()
+    for i in range(2):
+        path.run_from_host(w_host, g_host, p_host, stream, adam_step=1 + i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    h2d = d2h = 0
+    for i in range(steps):
+        h2d, d2h = path.run_from_host(w_host, g_host, p_host, stream, adam_step=3 + i)
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    if world > 1:
+        t = torch.tensor([dt], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": step_bytes * world / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps,
+            "note": "pinned host inputs copied in and bf16 parameters copied out every step, "
+                    "wall clock around the steps; value counts the same algorithmic bytes"}
+
+
+# ---- the oracle (CPU baseline and reference arm) --------------------------------------------
+
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle: the first `nbw`
+    blocks of every rank's weight shard (first qwZ call) and the first `nbg`
+    blocks of every slice of every rank's bucket -- a self-contained smaller
+    instance of the same pass (same topology, block, bits, Adam)."""
+
+    def __init__(self, wl, nbw, nbg):
+        import numpy as np
+        import synth
+        from synth import workloads as W
+        self.wl = wl
+        self.steps_bytes = 0
+        q, g = wl.qwz, wl.qgz
+        self.q = self.g = None
+        if q is not None:
+            nbw = max(1, min(nbw, -(-q.shard // q.block)))
+            n = min(q.shard, nbw * q.block)
+            idx = (np.arange(q.nranks)[:, None] * q.shard + np.arange(n)[None, :]).reshape(-1)
+            self.wx = synth.bf16_to_u16(synth.at(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, idx))
+            self.q = (q.nranks, n, q.block, q.bits)
+            m = q.nranks * msg_bytes(n, q.block, q.bits)
+            self.steps_bytes += 2 * (2 * q.nranks * n + m)
+        if g is not None:
+            nbg = max(1, min(nbg, g.slice_elems // g.block))
+            Lm = nbg * g.block
+            nd = g.nd
+            pos = (np.arange(nd)[:, None] * g.slice_elems + np.arange(Lm)[None, :]).reshape(-1)
+            self.gx = np.concatenate([synth.bf16_to_u16(
+                synth.at(g.grad, wl.seed, synth.grad_stream(r), pos)) for r in range(nd)])
+            bucket = nd * Lm
+            self.g = (g.nodes, g.gpus_per_node, bucket, g.block, g.bits)
+            gidx = (np.arange(nd)[:, None] * g.slice_elems + np.arange(Lm)[None, :]).reshape(-1)
+            import oracle
+            self.master = oracle.bf16_bits_to_f32(synth.bf16_to_u16(
+                synth.at(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, gidx)))
+            self.zero = np.zeros(bucket, np.float32)
+            m1 = nd * msg_bytes(bucket, g.block, g.bits)
+            b = m1 + 2 * nd * bucket
+            if g.nodes == 1:
+                b += m1
+            else:
+                m2 = nd * msg_bytes(g.nodes * Lm, g.block, g.bits)
+                b += m1 + m2 + m2
+            b += (26 if wl.fused_adam else 4) * bucket
+            self.steps_bytes += b
+            self.elems = nd * bucket
+
+    def run(self):
+        import oracle
+        if self.q is not None:
+            c, s = oracle.qwz_quant(self.wx, *self.q)
+            oracle.qwz_dequant(c, s, *self.q)
+        if self.g is not None:
+            gr = oracle.qgz_reduce_scatter(self.gx, *self.g)
+            if self.wl.fused_adam:
+                a = self.wl.adam
+                oracle.adam_step(gr, self.master, self.zero, self.zero, a.lr, a.beta1, a.beta2,
+                                 a.eps, a.step)
+
+
+def sized_sample(wl, seconds):
+    """Calibrate the sample so one oracle pass takes about `seconds`."""
+    s = OracleSample(wl, 4, 2)
+    t = time.perf_counter()
+    s.run()
+    dt = max(time.perf_counter() - t, 1e-4)
+    scale = max(1.0, seconds / dt)
+    return OracleSample(wl, int(4 * scale), int(2 * scale))
+
+
+def cpu_baseline(wl, seconds=12.0):
+    s = sized_sample(wl, seconds / 2)
+    t = time.perf_counter()
+    n = 0
+    while True:
+        s.run()
+        n += 1
+        if time.perf_counter() - t >= seconds / 2 and n >= 1:
+            break
+    dt = (time.perf_counter() - t) / n
+    return {"value": s.steps_bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{s.steps_bytes / 1e6:.1f} MB of algorithmic traffic per pass: the first "
+                      f"blocks of every shard and of every slice of every rank (same topology, "
+                      f"block, bits, Adam), {n} passes, single-threaded C oracle",
+            "seconds": dt * n}
+
+
+def run_reference(args, wl):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    budget = 150.0
+    per_step = max(0.2, min(5.0, budget / max(1, args.steps + args.warmup)))
+    s = sized_sample(wl, per_step)
+    for _ in range(args.warmup):
+        s.run()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        s.run()
+    dt = (time.perf_counter() - t) / args.steps
+    value = s.steps_bytes / dt / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded counter-based generator, bounded sample of the workload",
+        "config": workload_config(wl, args.config),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{s.steps_bytes / 1e6:.1f} MB of algorithmic traffic per "
+                                   "step: the first blocks of every shard and slice of every "
+                                   "rank, single-threaded C oracle"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---- main ------------------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama", choices=["tiny", "llama", "two_hop", "7b"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    from synth import workloads as W
+    wl = W.WORKLOADS[args.config]
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, wl)), flush=True)
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    try:
+        res = run_gpu(args, wl, rank, world, device)
+        if rank == 0 and world == 1 and not args.no_cpu:
+            res["cpu_baseline"] = cpu_baseline(wl)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+"""ctypes binding of libzpp.so: the C ABI of include/zpp.h, one Python function
+per entry point with the same name.  Argument marshalling only -- every step
+of the path runs in the CUDA kernels behind these calls.
+
+Tensors are passed as torch tensors on a CUDA device (contiguous, of the dtype
+the header states) and turned into raw device pointers; `stream` defaults to
+torch's current stream on the tensors' device.  A nonzero status raises
+``ZppError``.  If the library has not been built the first call raises: there
+is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB
+
+ZPP_OK, ZPP_ERR_INVALID_ARG, ZPP_ERR_MISALIGNED, ZPP_ERR_UNSUPPORTED, ZPP_ERR_CUDA = range(5)
+
+# every symbol include/zpp.h declares
+EXPORTS = (
+    "zpp_qwz_quant", "zpp_qwz_dequant", "zpp_qgz_reorder_quant", "zpp_qgz_hop_reduce",
+    "zpp_shard_adam_step", "zpp_codes_bytes", "zpp_num_blocks", "zpp_qgz_slice_perm",
+    "zpp_status_string", "zpp_last_cuda_error", "zpp_abi_version",
+)
+
+
+class ZppError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib().zpp_status_string(status).decode()
+        if status == ZPP_ERR_CUDA:
+            msg += ": " + _lib().zpp_last_cuda_error().decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+class zpp_adam_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("step", ctypes.c_int32)]
+
+
+class zpp_adam_state(ctypes.Structure):
+    _fields_ = [("master", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("param_bf16", ctypes.c_void_p)]
+
+
+_handle = None
+
+
+def library_path() -> str:
+    return LIB
+
+
+def _lib():
+    global _handle
+    if _handle is not None:
+        return _handle
+    if not os.path.exists(LIB):
+        raise RuntimeError(
+            f"{LIB} is not built: run `python -m gradient_comm_codecs_gb300._build` "
+            "(or __graft_entry__.build()) first; there is no fallback implementation")
+    lib = ctypes.CDLL(LIB)
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    HP, ST = ctypes.POINTER(zpp_adam_hparams), ctypes.POINTER(zpp_adam_state)
+    sigs = {
+        "zpp_qwz_quant": (I32, [P, I64, I64, I32, I32, P, P, P]),
+        "zpp_qwz_dequant": (I32, [P, P, I64, I64, I32, I32, P, P]),
+        "zpp_qgz_reorder_quant": (I32, [P, I32, I32, I64, I32, I32, P, P, P]),
+        "zpp_qgz_hop_reduce": (I32, [I32, P, P, I32, I32, I64, I32, I32, P, P, P, HP, ST, P]),
+        "zpp_shard_adam_step": (I32, [P, I64, HP, ST, P]),
+        "zpp_codes_bytes": (I64, [I64, I32]),
+        "zpp_num_blocks": (I64, [I64, I32]),
+        "zpp_qgz_slice_perm": (I32, [I32, I32, P]),
+        "zpp_status_string": (ctypes.c_char_p, [I32]),
+        "zpp_last_cuda_error": (ctypes.c_char_p, []),
+        "zpp_abi_version": (I32, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    _handle = lib
+    return lib
+
+
+# ---- marshalling helpers ----------------------------------------------------------
+
+def _dev(t, dtype, name):
+    """Raw device pointer of a tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):  # already a raw device pointer
+        return t
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch tensor or a device pointer")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: tensor must be on a CUDA device")
+    if dtype is not None and t.dtype not in dtype:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: tensor must be contiguous")
+    return t.data_ptr()
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (
+    torch.bfloat16, torch.int16)
+_BYTES = (torch.uint8, torch.int8)
+_F32 = (torch.float32,)
+
+
+def _stream(stream, *tensors):
+    if stream is None:
+        dev = next((t.device for t in tensors if isinstance(t, torch.Tensor)), None)
+        return torch.cuda.current_stream(dev).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status, where):
+    if status != ZPP_OK:
+        raise ZppError(status, where)
+
+
+# ---- entry points ---------------------------------------------------------------------
+
+def zpp_qwz_quant(x_bf16, nranks, shard_elems, block, bits, codes, scales, stream=None):
+    _check(_lib().zpp_qwz_quant(_dev(x_bf16, _BF16, "x_bf16"), nranks, shard_elems, block, bits,
+                                _dev(codes, _BYTES, "codes"), _dev(scales, _F32, "scales"),
+                                _stream(stream, x_bf16)), "zpp_qwz_quant")
+
+
+def zpp_qwz_dequant(codes, scales, nranks, shard_elems, block, bits, y_bf16, stream=None):
+    _check(_lib().zpp_qwz_dequant(_dev(codes, _BYTES, "codes"), _dev(scales, _F32, "scales"),
+                                  nranks, shard_elems, block, bits, _dev(y_bf16, _BF16, "y_bf16"),
+                                  _stream(stream, codes)), "zpp_qwz_dequant")
+
+
+def zpp_qgz_reorder_quant(grads_bf16, nodes, gpus_per_node, bucket_elems, block, bits, codes,
+                          scales, stream=None):
+    _check(_lib().zpp_qgz_reorder_quant(_dev(grads_bf16, _BF16, "grads_bf16"), nodes,
+                                        gpus_per_node, bucket_elems, block, bits,
+                                        _dev(codes, _BYTES, "codes"), _dev(scales, _F32, "scales"),
+                                        _stream(stream, grads_bf16)), "zpp_qgz_reorder_quant")
+
+
+def _adam_args(adam, state):
+    hp = st = None
+    if adam is not None:
+        hp = zpp_adam_hparams(*adam) if isinstance(adam, (tuple, list)) else adam
+    if state is not None:
+        if isinstance(state, (tuple, list)):
+            master, m, v, param = state
+            st = zpp_adam_state(_dev(master, _F32, "master"), _dev(m, _F32, "m"),
+                                _dev(v, _F32, "v"), _dev(param, _BF16, "param_bf16"))
+        else:
+            st = state
+    return (ctypes.byref(hp) if hp is not None else None,
+            ctypes.byref(st) if st is not None else None, hp, st)
+
+
+def zpp_qgz_hop_reduce(hop, codes_in, scales_in, nodes, gpus_per_node, bucket_elems, block, bits,
+                       codes_out=None, scales_out=None, grad_out=None, adam=None, state=None,
+                       stream=None):
+    """`adam`: (lr, beta1, beta2, eps, step) or zpp_adam_hparams; `state`:
+    (master, m, v, param_bf16_or_None) tensors or zpp_adam_state."""
+    hp, st, _keep1, _keep2 = _adam_args(adam, state)
+    _check(_lib().zpp_qgz_hop_reduce(hop, _dev(codes_in, _BYTES, "codes_in"),
+                                     _dev(scales_in, _F32, "scales_in"), nodes, gpus_per_node,
+                                     bucket_elems, block, bits,
+                                     _dev(codes_out, _BYTES, "codes_out"),
+                                     _dev(scales_out, _F32, "scales_out"),
+                                     _dev(grad_out, _F32, "grad_out"), hp, st,
+                                     _stream(stream, codes_in)), "zpp_qgz_hop_reduce")
+
+
+def zpp_shard_adam_step(grad, n, adam, state, stream=None):
+    hp, st, _keep1, _keep2 = _adam_args(adam, state)
+    _check(_lib().zpp_shard_adam_step(_dev(grad, _F32, "grad"), n, hp, st, _stream(stream, grad)),
+           "zpp_shard_adam_step")
+
+
+def zpp_codes_bytes(n, bits):
+    return int(_lib().zpp_codes_bytes(n, bits))
+
+
+def zpp_num_blocks(n, block):
+    return int(_lib().zpp_num_blocks(n, block))
+
+
+def zpp_qgz_slice_perm(nodes, gpus_per_node):
+    arr = (ctypes.c_int32 * (nodes * gpus_per_node))()
+    _check(_lib().zpp_qgz_slice_perm(nodes, gpus_per_node, arr), "zpp_qgz_slice_perm")
+    return list(arr)
+
+
+def zpp_status_string(status):
+    return _lib().zpp_status_string(status).decode()
+
+
+def zpp_abi_version():
+    return int(_lib().zpp_abi_version())

@@ -1,0 +1,57 @@
+// zpp_launch.h -- host-side launchers of the ZeRO++ codec kernels.  Called by
+// the C ABI (zpp_abi.cu) after it has validated every argument; each launcher
+// only shapes the grid and enqueues on `stream`.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace zpp {
+
+constexpr int kThreads = 256;  // threads per CTA of every kernel
+
+struct AdamConstsHost {
+  float lr, beta1, beta2, eps, omb1, omb2, bc1, bc2;
+};
+
+// Row-blocked quantization of bf16 rows.
+//  qwZ   : rows = nranks, row r = x[r*shard .. +shard), codes/scales per rank.
+//  qgZ   : rows = N_d * N_d (rank, slice); slice j of rank r goes to message
+//          position p = (j % G) * N + j / G.
+cudaError_t launch_qwz_quant(const uint16_t* x, int64_t nranks, int64_t shard, int32_t block,
+                             int32_t bits, void* codes, float* scales, cudaStream_t st);
+cudaError_t launch_qgz_reorder_quant(const uint16_t* x, int32_t N, int32_t G, int64_t bucket,
+                                     int32_t block, int32_t bits, void* codes, float* scales,
+                                     cudaStream_t st);
+cudaError_t launch_qwz_dequant(const void* codes, const float* scales, int64_t nranks,
+                               int64_t shard, int32_t block, int32_t bits, uint16_t* y,
+                               cudaStream_t st);
+
+// One hop of the hierarchical reduce (see zpp_qgz_hop_reduce).
+struct HopLaunch {
+  int32_t hop;            // 1 or 2
+  const void* codes_in;
+  const float* scales_in;
+  int32_t N, G;
+  int64_t bucket;
+  int32_t block, bits;
+  void* codes_out;        // non-final hop
+  float* scales_out;
+  float* grad_out;        // final hop, optional
+  float inv_nd;
+  bool adam;              // final hop: fused Adam
+  AdamConstsHost ac;
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* param;
+};
+cudaError_t launch_hop_reduce(const HopLaunch& h, cudaStream_t st);
+
+cudaError_t launch_adam(const float* grad, int64_t n, const AdamConstsHost& ac, float* master,
+                        float* m, float* v, uint16_t* param, cudaStream_t st);
+
+// Grid size for a kernel: min(work CTAs, SMs * resident CTAs per SM).
+int grid_for(const void* kernel, int64_t work_ctas, size_t smem = 0);
+
+}  // namespace zpp

@@ -1,0 +1,197 @@
+"""Device buffers and call sequence of one pass of the ZeRO++ data-parallel path.
+
+Plumbing only: allocates the simulated ranks' buffers with torch and issues
+the C-ABI calls in order.  One pass (``CodecPath.run``) is
+
+  qwZ   zpp_qwz_quant (every rank's weight shard) -> zpp_qwz_dequant (the
+        all-gather receiver, one full bf16 copy), optionally over several
+        chunks of a long weight tensor;
+  qgZ   zpp_qgz_reorder_quant (every rank's bucket) -> zpp_qgz_hop_reduce(1)
+        -> zpp_qgz_hop_reduce(2) when there is more than one node, the final
+        hop applying the Adam step to every rank's owned slice.
+
+Every message between two calls is a separate HBM buffer, as the wire
+between two GPUs would be.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib as Z
+
+
+@dataclass(frozen=True)
+class QwzSpec:
+    nranks: int
+    shard: int
+    block: int
+    bits: int = 8
+    chunks: int = 1          # the weight tensor is `chunks` calls of nranks*shard
+    tail_shard: int = 0      # shard of the last call when nonzero
+
+    def call_shards(self):
+        s = [self.shard] * self.chunks
+        if self.tail_shard:
+            s[-1] = self.tail_shard
+        return s
+
+    @property
+    def phi(self):
+        return self.nranks * sum(self.call_shards())
+
+
+@dataclass(frozen=True)
+class QgzSpec:
+    nodes: int
+    gpus_per_node: int
+    bucket: int
+    block: int
+    bits: int = 4
+
+    @property
+    def nd(self):
+        return self.nodes * self.gpus_per_node
+
+    @property
+    def L(self):
+        return self.bucket // self.nd
+
+
+@dataclass(frozen=True)
+class AdamSpec:
+    lr: float = 1e-4
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    step: int = 1
+
+    def hparams(self):
+        return (self.lr, self.beta1, self.beta2, self.eps, self.step)
+
+
+def _empty(n, dtype, device):
+    return torch.empty(int(n), dtype=dtype, device=device)
+
+
+class CodecPath:
+    """Buffers of one simulated ZeRO++ step on one device.
+
+    Inputs the caller fills: ``w`` (bf16 weights, all calls concatenated),
+    ``grads`` (bf16 [N_d][bucket]) and the Adam state ``master, m, v``
+    (fp32 [bucket], element r*L + i owned by rank r).
+    """
+
+    def __init__(self, qwz: QwzSpec | None, qgz: QgzSpec | None, adam: AdamSpec | None,
+                 device="cuda", keep_grad: bool = False, write_param: bool = True):
+        self.qwz, self.qgz, self.adam = qwz, qgz, adam
+        self.device = torch.device(device)
+        dev = self.device
+        self.launches_per_run = 0
+        if qwz is not None:
+            self.w = _empty(qwz.phi, torch.bfloat16, dev)
+            shards = qwz.call_shards()
+            self.w_codes = [_empty(qwz.nranks * Z.zpp_codes_bytes(s, qwz.bits), torch.uint8, dev)
+                            for s in sorted(set(shards))]
+            self._codes_of = {s: i for i, s in enumerate(sorted(set(shards)))}
+            self.w_scales = [_empty(qwz.nranks * Z.zpp_num_blocks(s, qwz.block), torch.float32, dev)
+                             for s in sorted(set(shards))]
+            self.w_full = _empty(qwz.phi, torch.bfloat16, dev)
+            self.launches_per_run += 2 * len(shards)
+        if qgz is not None:
+            nd, b = qgz.nd, qgz.bucket
+            self.grads = _empty(nd * b, torch.bfloat16, dev)
+            self.msg1 = _empty(nd * Z.zpp_codes_bytes(b, qgz.bits), torch.uint8, dev)
+            self.msg1_scales = _empty(nd * (b // qgz.block), torch.float32, dev)
+            self.launches_per_run += 2
+            if qgz.nodes > 1:
+                nl = qgz.nodes * qgz.L
+                self.msg2 = _empty(nd * Z.zpp_codes_bytes(nl, qgz.bits), torch.uint8, dev)
+                self.msg2_scales = _empty(nd * (nl // qgz.block), torch.float32, dev)
+                self.launches_per_run += 1
+            self.grad_out = _empty(b, torch.float32, dev) if (keep_grad or adam is None) else None
+            if adam is not None:
+                self.master = _empty(b, torch.float32, dev)
+                self.m = torch.zeros(b, dtype=torch.float32, device=dev)
+                self.v = torch.zeros(b, dtype=torch.float32, device=dev)
+                self.param = _empty(b, torch.bfloat16, dev) if write_param else None
+
+    # ---- the pass ---------------------------------------------------------------
+    # `mark(name)`, when given, is called after each launch (the bench records a
+    # CUDA event there to time every kernel of the pass).
+    def run_qwz(self, stream=None, mark=None):
+        q = self.qwz
+        off = 0
+        for s in q.call_shards():
+            n = q.nranks * s
+            i = self._codes_of[s]
+            x = self.w[off:off + n]
+            Z.zpp_qwz_quant(x, q.nranks, s, q.block, q.bits, self.w_codes[i], self.w_scales[i],
+                            stream)
+            if mark:
+                mark("qwz_quant")
+            Z.zpp_qwz_dequant(self.w_codes[i], self.w_scales[i], q.nranks, s, q.block, q.bits,
+                              self.w_full[off:off + n], stream)
+            if mark:
+                mark("qwz_dequant")
+            off += n
+
+    def run_qgz(self, stream=None, adam_step: int | None = None, mark=None):
+        g = self.qgz
+        Z.zpp_qgz_reorder_quant(self.grads, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits,
+                                self.msg1, self.msg1_scales, stream)
+        if mark:
+            mark("qgz_reorder_quant")
+        adam = state = None
+        if self.adam is not None:
+            hp = list(self.adam.hparams())
+            if adam_step is not None:
+                hp[4] = adam_step
+            adam = tuple(hp)
+            state = (self.master, self.m, self.v, self.param)
+        if g.nodes == 1:
+            Z.zpp_qgz_hop_reduce(1, self.msg1, self.msg1_scales, g.nodes, g.gpus_per_node,
+                                 g.bucket, g.block, g.bits, grad_out=self.grad_out, adam=adam,
+                                 state=state, stream=stream)
+            if mark:
+                mark("qgz_final_hop")
+        else:
+            Z.zpp_qgz_hop_reduce(1, self.msg1, self.msg1_scales, g.nodes, g.gpus_per_node,
+                                 g.bucket, g.block, g.bits, codes_out=self.msg2,
+                                 scales_out=self.msg2_scales, stream=stream)
+            if mark:
+                mark("qgz_hop1")
+            Z.zpp_qgz_hop_reduce(2, self.msg2, self.msg2_scales, g.nodes, g.gpus_per_node,
+                                 g.bucket, g.block, g.bits, grad_out=self.grad_out, adam=adam,
+                                 state=state, stream=stream)
+            if mark:
+                mark("qgz_final_hop")
+
+    def run(self, stream=None, adam_step: int | None = None, mark=None):
+        if self.qwz is not None:
+            self.run_qwz(stream, mark)
+        if self.qgz is not None:
+            self.run_qgz(stream, adam_step, mark)
+
+    def run_from_host(self, w_host=None, grads_host=None, param_host=None, stream=None,
+                      adam_step: int | None = None):
+        """One pass on host-resident data: copy this step's weights and
+        gradients in (pinned host tensors, asynchronous on `stream`), run, and
+        copy the updated 16-bit parameters back.  Returns the bytes moved each
+        way (h2d, d2h)."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        h2d = d2h = 0
+        with torch.cuda.stream(s):
+            if w_host is not None:
+                self.w.copy_(w_host, non_blocking=True)
+                h2d += w_host.numel() * w_host.element_size()
+            if grads_host is not None:
+                self.grads.copy_(grads_host, non_blocking=True)
+                h2d += grads_host.numel() * grads_host.element_size()
+            self.run(s.cuda_stream, adam_step)
+            if param_host is not None:
+                src = self.param if self.param is not None else self.master
+                param_host.copy_(src, non_blocking=True)
+                d2h += param_host.numel() * param_host.element_size()
+        return h2d, d2h

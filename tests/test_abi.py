@@ -1,0 +1,152 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+symbol include/zpp.h declares; host-only helpers; argument validation (which
+returns before anything touches the device)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gradient_comm_codecs_gb300 import _build, _lib
+    _build.build()
+    return _lib._lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "zpp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(zpp_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    fns = header_functions()
+    for name in ("zpp_qwz_quant", "zpp_qwz_dequant", "zpp_qgz_reorder_quant",
+                 "zpp_qgz_hop_reduce", "zpp_shard_adam_step"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from gradient_comm_codecs_gb300 import EXPORTS
+    fns = header_functions()
+    assert sorted(EXPORTS) == fns
+    for name in fns:
+        assert hasattr(lib, name), name
+    # the binding refers to nothing the header does not declare
+    out = os.popen(f"nm -D --defined-only {lib._name}").read()
+    exported = set(re.findall(r"\bT (zpp_[a-z0-9_]+)\b", out))
+    assert set(fns) <= exported
+
+
+def test_size_helpers(lib):
+    import gradient_comm_codecs_gb300 as Z
+    import oracle
+    for n in (0, 1, 2, 7, 255, 256, 257, 10 ** 9 + 3):
+        for bits in (4, 8):
+            if bits == 4 and n % 2:
+                continue
+            assert Z.zpp_codes_bytes(n, bits) == oracle.codes_bytes(n, bits)
+        for block in (64, 256, 4096):
+            assert Z.zpp_num_blocks(n, block) == oracle.num_blocks(n, block)
+    assert Z.zpp_codes_bytes(-1, 8) == -1 and Z.zpp_codes_bytes(10, 3) == -1
+    assert Z.zpp_num_blocks(10, 0) == -1
+
+
+def test_slice_perm_matches_oracle(lib):
+    import gradient_comm_codecs_gb300 as Z
+    import oracle
+    for N in range(1, 9):
+        for G in range(1, 9):
+            assert Z.zpp_qgz_slice_perm(N, G) == list(oracle.qgz_slice_perm(N, G))
+    with pytest.raises(Z.ZppError):
+        Z.zpp_qgz_slice_perm(0, 4)
+
+
+def test_status_strings_and_version(lib):
+    import gradient_comm_codecs_gb300 as Z
+    assert Z.zpp_status_string(0) == "ok"
+    assert "aligned" in Z.zpp_status_string(2)
+    assert Z.zpp_abi_version() >> 16 == 1
+    assert lib.zpp_last_cuda_error() == b""
+
+
+A = 1 << 20          # a fake, 16-byte aligned "device pointer" value: never dereferenced
+M = A + 8            # misaligned
+
+
+def test_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    E_ARG, E_MIS = 1, 2
+    # qwZ
+    assert lib.zpp_qwz_quant(P(A), 4, 256, 256, 3, P(A), P(A), None) == E_ARG     # bits
+    assert lib.zpp_qwz_quant(P(A), 4, 256, 100, 8, P(A), P(A), None) == E_ARG     # block not pow2
+    assert lib.zpp_qwz_quant(P(A), 4, 256, 32, 8, P(A), P(A), None) == E_ARG      # block < 64
+    assert lib.zpp_qwz_quant(P(A), 4, 256, 8192, 8, P(A), P(A), None) == E_ARG    # block > 4096
+    assert lib.zpp_qwz_quant(P(A), 4, 255, 256, 4, P(A), P(A), None) == E_ARG     # odd int4 shard
+    assert lib.zpp_qwz_quant(P(A), -1, 256, 256, 8, P(A), P(A), None) == E_ARG
+    assert lib.zpp_qwz_quant(None, 4, 256, 256, 8, P(A), P(A), None) == E_ARG
+    assert lib.zpp_qwz_quant(P(M), 4, 256, 256, 8, P(A), P(A), None) == E_MIS
+    assert lib.zpp_qwz_quant(P(A), 4, 256, 256, 8, P(M), P(A), None) == E_MIS
+    assert lib.zpp_qwz_quant(None, 0, 256, 256, 8, None, None, None) == 0         # empty: no-op
+    assert lib.zpp_qwz_quant(None, 4, 0, 256, 8, None, None, None) == 0
+    assert lib.zpp_qwz_dequant(P(A), P(A), 4, 256, 256, 8, P(M), None) == E_MIS
+    assert lib.zpp_qwz_dequant(P(A), P(A), 4, 3, 256, 4, P(A), None) == E_ARG
+    # qgZ reorder
+    assert lib.zpp_qgz_reorder_quant(P(A), 2, 2, 4 * 256 + 4, 256, 4, P(A), P(A), None) == E_ARG
+    assert lib.zpp_qgz_reorder_quant(P(A), 0, 2, 4096, 256, 4, P(A), P(A), None) == E_ARG
+    assert lib.zpp_qgz_reorder_quant(P(A), 2, 2, 4096, 256, 5, P(A), P(A), None) == E_ARG
+    assert lib.zpp_qgz_reorder_quant(P(M), 2, 2, 4096, 256, 4, P(A), P(A), None) == E_MIS
+    assert lib.zpp_qgz_reorder_quant(None, 2, 2, 0, 256, 4, None, None, None) == 0
+
+
+def test_hop_validation(lib):
+    from gradient_comm_codecs_gb300._lib import zpp_adam_hparams, zpp_adam_state
+    P = ctypes.c_void_p
+    hp = zpp_adam_hparams(1e-4, 0.9, 0.999, 1e-8, 1)
+    bad_hp = zpp_adam_hparams(1e-4, 0.9, 0.999, 1e-8, 0)
+    st = zpp_adam_state(A, A, A, A)
+    st_mis = zpp_adam_state(A, M, A, A)
+    st_null = zpp_adam_state(A, None, A, A)
+    f = lib.zpp_qgz_hop_reduce
+    b = 4 * 256 * 4
+    ref = ctypes.byref
+    # hop 2 with one node: hop 1 is final
+    assert f(2, P(A), P(A), 1, 4, b, 256, 4, None, None, P(A), None, None, None) == 1
+    # hop 3
+    assert f(3, P(A), P(A), 2, 2, b, 256, 4, P(A), P(A), None, None, None, None) == 1
+    # non-final hop: needs codes_out and scales_out, and nothing final
+    assert f(1, P(A), P(A), 2, 2, b, 256, 4, None, P(A), None, None, None, None) == 1
+    assert f(1, P(A), P(A), 2, 2, b, 256, 4, P(A), P(A), P(A), None, None, None) == 1
+    assert f(1, P(A), P(A), 2, 2, b, 256, 4, P(A), P(A), None, ref(hp), ref(st), None) == 1
+    # final hop: needs grad_out or adam, no codes_out
+    assert f(2, P(A), P(A), 2, 2, b, 256, 4, None, None, None, None, None, None) == 1
+    assert f(2, P(A), P(A), 2, 2, b, 256, 4, P(A), None, P(A), None, None, None) == 1
+    assert f(1, P(A), P(A), 1, 4, b, 256, 4, None, None, None, ref(hp), None, None) == 1
+    assert f(1, P(A), P(A), 1, 4, b, 256, 4, None, None, None, ref(bad_hp), ref(st), None) == 1
+    assert f(1, P(A), P(A), 1, 4, b, 256, 4, None, None, None, ref(hp), ref(st_null), None) == 1
+    assert f(1, P(A), P(A), 1, 4, b, 256, 4, None, None, None, ref(hp), ref(st_mis), None) == 2
+    assert f(2, P(A), P(A), 2, 2, b, 256, 4, None, None, P(M), None, None, None) == 2
+    # bucket not a multiple of N_d * block
+    assert f(2, P(A), P(A), 2, 2, b + 256, 256, 4, None, None, P(A), None, None, None) == 1
+    # empty bucket: valid no-op
+    assert f(2, None, None, 2, 2, 0, 256, 4, None, None, P(A), None, None, None) == 0
+    # Adam
+    g = lib.zpp_shard_adam_step
+    assert g(P(A), 100, ref(bad_hp), ref(st), None) == 1
+    assert g(P(A), 100, ref(hp), ref(st_null), None) == 1
+    assert g(P(M), 100, ref(hp), ref(st), None) == 2
+    assert g(P(A), -5, ref(hp), ref(st), None) == 1
+    assert g(None, 0, ref(hp), ref(st), None) == 0
+
+
+def test_binding_rejects_host_tensors():
+    import torch
+    import gradient_comm_codecs_gb300 as Z
+    x = torch.zeros(1024, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        Z.zpp_qwz_quant(x, 1, 1024, 256, 8, x, x, stream=0)

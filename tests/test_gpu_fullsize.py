@@ -1,0 +1,223 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+bench times (CodecPath), on sampled outputs the oracle recomputes one by one.
+
+Inputs are generated on the device by the counter-based generator; the host
+regenerates exactly the elements a sampled output depends on.  For qgZ a
+sampled block position b of every slice is a self-contained sub-problem: its
+one-shot codes, hop-1 partial sums and final gradient depend only on block b
+of every rank's slices, so the oracle runs the whole chain on a "mini bucket"
+made of the sampled blocks of all slices of all ranks and every rank's
+message, hop-1 message, reduced gradient and Adam state is compared there.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import workloads as W
+from gpu_helpers import (assert_bf16_ulp, assert_bytes_equal, assert_f32_bitexact,
+                         assert_grad_close, assert_rel_close, grads_for, zpp)
+
+pytestmark = pytest.mark.gpu
+
+
+def gather_bytes(t: torch.Tensor, starts, length):
+    """Bytes [s, s + length) of a flat uint8 device tensor for every start s."""
+    idx = (torch.as_tensor(np.asarray(starts, np.int64))[:, None]
+           + torch.arange(length, dtype=torch.int64)[None, :]).reshape(-1).to(t.device)
+    return t.index_select(0, idx).cpu().numpy()
+
+
+def gather_f32(t: torch.Tensor, idx):
+    return t.index_select(0, torch.as_tensor(np.asarray(idx, np.int64)).to(t.device)).cpu().numpy()
+
+
+def gather_u16(t: torch.Tensor, idx):
+    v = t.index_select(0, torch.as_tensor(np.asarray(idx, np.int64)).to(t.device))
+    return synth.bf16_to_u16(v)
+
+
+def sample_blocks(nblocks, k, seed):
+    rng = np.random.default_rng(seed)
+    picks = {0, nblocks - 1}
+    picks.update(int(x) for x in rng.integers(0, nblocks, size=k))
+    return sorted(picks)
+
+
+def build_path(Z, wl: W.Workload, keep_grad=True):
+    q, g = wl.qwz, wl.qgz
+    qs = gs = None
+    if q is not None:
+        qs = Z.QwzSpec(q.nranks, q.shard, q.block, q.bits, chunks=q.calls, tail_shard=q.tail_shard)
+    if g is not None:
+        gs = Z.QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+    a = wl.adam
+    adam = Z.AdamSpec(a.lr, a.beta1, a.beta2, a.eps, a.step) if (g and wl.fused_adam) else None
+    path = Z.CodecPath(qs, gs, adam, device="cuda", keep_grad=keep_grad)
+    if q is not None:
+        synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, qs.phi, out=path.w)
+    if g is not None:
+        path.grads.copy_(grads_for(g, wl.seed, device="cuda"))
+        if adam is not None:
+            m = synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, g.bucket, device="cuda")
+            path.master.copy_(m.float())
+            del m
+    return path
+
+
+def check_qwz(path, wl, nsample=3):
+    q = wl.qwz
+    B, bits = q.block, q.bits
+    off = 0
+    for call, s in enumerate(path.qwz.call_shards()):
+        i = path._codes_of[s]
+        codes, scales = path.w_codes[i], path.w_scales[i]
+        nb = -(-s // B)
+        cb = oracle.codes_bytes(s, bits)
+        for r in sorted({0, q.nranks - 1}):
+            for b in sample_blocks(nb, nsample, 1000 * call + r):
+                n = min(B, s - b * B)
+                gidx = off + r * s + b * B + np.arange(n)
+                x = synth.bf16_to_u16(synth.at(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, gidx))
+                wc, ws = oracle.qwz_quant(x, 1, n, B, bits)
+                wy = oracle.qwz_dequant(wc, ws, 1, n, B, bits)
+                got_c = gather_bytes(codes, [r * cb + (b * B * bits) // 8], wc.size)
+                assert_bytes_equal(got_c, wc, f"qwZ codes call {call} rank {r} block {b}")
+                got_s = gather_f32(scales, [r * nb + b])
+                assert_f32_bitexact(got_s, ws, f"qwZ scale call {call} rank {r} block {b}")
+                assert_bytes_equal(gather_u16(path.w_full, gidx), wy, f"qwZ dequant {call}/{r}/{b}")
+        # only a few calls of a long tensor: first, last, one in between
+        off += q.nranks * s
+
+
+def check_qgz(path, wl, nsample=2):
+    g = wl.qgz
+    N, G, B, bits = g.nodes, g.gpus_per_node, g.block, g.bits
+    Nd, L, bucket = g.nd, g.slice_elems, g.bucket
+    blocks = sample_blocks(L // B, nsample, 7)
+    nbk = len(blocks)
+    Lm = nbk * B
+    # mini bucket: rank r, slice j, sampled block q
+    pos = (np.arange(Nd)[:, None, None] * L + np.asarray(blocks)[None, :, None] * B
+           + np.arange(B)[None, None, :]).reshape(-1)            # slice-relative index j*L + b*B + e
+    mini = np.empty(Nd * Nd * Lm, np.uint16)
+    for r in range(Nd):
+        mini[r * Nd * Lm:(r + 1) * Nd * Lm] = synth.bf16_to_u16(
+            synth.at(g.grad, wl.seed, synth.grad_stream(r), pos))
+    c1, s1 = oracle.qgz_reorder_quant(mini, N, G, Nd * Lm, B, bits)
+    perm = oracle.qgz_slice_perm(N, G)
+    cbr, cbm = oracle.codes_bytes(bucket, bits), oracle.codes_bytes(Nd * Lm, bits)
+    bb = B * bits // 8
+    # one-shot messages of every rank at every slice position
+    starts, wstarts, sidx, widx = [], [], [], []
+    for r in range(Nd):
+        for p in range(Nd):
+            for qi, b in enumerate(blocks):
+                starts.append(r * cbr + ((p * L + b * B) * bits) // 8)
+                wstarts.append(r * cbm + ((p * Lm + qi * B) * bits) // 8)
+                sidx.append(r * (bucket // B) + (p * L + b * B) // B)
+                widx.append(r * (Nd * Lm // B) + p * nbk + qi)
+    got = gather_bytes(path.msg1, starts, bb)
+    want = c1.reshape(-1)[(np.asarray(wstarts)[:, None] + np.arange(bb)[None, :]).reshape(-1)]
+    assert_bytes_equal(got, want, "one-shot codes")
+    assert_f32_bitexact(gather_f32(path.msg1_scales, sidx), s1[widx], "one-shot scales")
+    assert perm is not None
+    if N == 1:
+        gref = oracle.qgz_hop1(c1, s1, N, G, Nd * Lm, B, bits)
+    else:
+        c2, s2 = oracle.qgz_hop1(c1, s1, N, G, Nd * Lm, B, bits)
+        NL, NLm = N * L, N * Lm
+        cb2, cb2m = oracle.codes_bytes(NL, bits), oracle.codes_bytes(NLm, bits)
+        starts, wstarts, sidx, widx = [], [], [], []
+        for d in range(Nd):
+            for k in range(N):
+                for qi, b in enumerate(blocks):
+                    starts.append(d * cb2 + ((k * L + b * B) * bits) // 8)
+                    wstarts.append(d * cb2m + ((k * Lm + qi * B) * bits) // 8)
+                    sidx.append(d * (NL // B) + (k * L + b * B) // B)
+                    widx.append(d * (NLm // B) + k * nbk + qi)
+        got = gather_bytes(path.msg2, starts, bb)
+        want = c2.reshape(-1)[(np.asarray(wstarts)[:, None] + np.arange(bb)[None, :]).reshape(-1)]
+        assert_bytes_equal(got, want, "hop-1 codes")
+        assert_f32_bitexact(gather_f32(path.msg2_scales, sidx), s2[widx], "hop-1 scales")
+        gref = oracle.qgz_hop2(c2, s2, N, G, Nd * Lm, B, bits)
+    # reduced gradient and Adam state of every rank's sampled blocks
+    gidx = (np.arange(Nd)[:, None, None] * L + np.asarray(blocks)[None, :, None] * B
+            + np.arange(B)[None, None, :]).reshape(-1)               # global parameter index
+    if path.grad_out is not None:
+        got_g = gather_f32(path.grad_out, gidx)
+        assert_grad_close(got_g, gref, B, "reduced gradient")
+        assert_f32_bitexact(got_g, gref, "reduced gradient (bit-exact)")
+    if path.adam is not None:
+        a = wl.adam
+        p0 = oracle.bf16_bits_to_f32(synth.bf16_to_u16(
+            synth.at(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, gidx)))
+        z = np.zeros(gidx.size, np.float32)
+        wp, wm, wv, wb = oracle.adam_step(gref, p0, z, z, a.lr, a.beta1, a.beta2, a.eps, a.step)
+        assert_rel_close(gather_f32(path.master, gidx), wp, 1e-5, "master")
+        assert_rel_close(gather_f32(path.m, gidx), wm, 1e-5, "m")
+        assert_rel_close(gather_f32(path.v, gidx), wv, 1e-5, "v")
+        assert_bf16_ulp(gather_u16(path.param, gidx), wb, "param")
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama", "two_hop", "7b"])
+def test_workload_full_size(name):
+    Z = zpp()
+    wl = W.WORKLOADS[name]
+    torch.cuda.empty_cache()
+    path = build_path(Z, wl)
+    path.run()
+    torch.cuda.synchronize()
+    if wl.qwz is not None:
+        check_qwz(path, wl)
+    if wl.qgz is not None:
+        check_qgz(path, wl)
+    del path
+    torch.cuda.empty_cache()
+
+
+def test_7b_standalone_adam_full_size():
+    """Standalone Adam on the 7B workload's 109,375,000-parameter owned shard."""
+    Z = zpp()
+    n = W.SEVEN_B.standalone_adam
+    g = synth.fill(W.GRAD_NORMAL, 3, synth.grad_stream(0), 0, n, device="cuda").float()
+    master = synth.fill(W.WEIGHT_RECIPE, 3, synth.WEIGHTS, 0, n, device="cuda").float()
+    m = synth.fill(W.MOMENT_M_RECIPE, 3, synth.MOMENT_M, 0, n, device="cuda").float()
+    v = synth.fill(W.MOMENT_V_RECIPE, 3, synth.MOMENT_V, 0, n, device="cuda").float()
+    param = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    hp = (1e-4, 0.9, 0.999, 1e-8, 7)
+    idx = np.unique(np.concatenate([np.arange(0, 1000), np.arange(n - 1000, n),
+                                    np.random.default_rng(5).integers(0, n, 20000)]))
+    g0, p0, m0, v0 = (gather_f32(t, idx) for t in (g, master, m, v))
+    Z.zpp_shard_adam_step(g, n, hp, (master, m, v, param))
+    torch.cuda.synchronize()
+    wp, wm, wv, wb = oracle.adam_step(g0, p0, m0, v0, *hp)
+    assert_rel_close(gather_f32(master, idx), wp, 1e-5, "master")
+    assert_rel_close(gather_f32(m, idx), wm, 1e-5, "m")
+    assert_rel_close(gather_f32(v, idx), wv, 1e-5, "v")
+    assert_bf16_ulp(gather_u16(param, idx), wb, "param")
+
+
+SWEEP_SAMPLE = [0, 7, 23, 30, 47, 53, 70, 95, 101, 118, 131, 141]
+
+
+@pytest.mark.parametrize("index", SWEEP_SAMPLE)
+def test_sweep_points(index):
+    """A spread of sweep points (every block size, both widths, every topology,
+    1 MiB to 1 GiB per rank where it fits), sampled as above, no Adam."""
+    Z = zpp()
+    wl = dict(W.sweep_points())[index]
+    need = wl.qgz.nd * wl.qgz.bucket * (2 + 2 * wl.qgz.bits / 8 + 8 / wl.qgz.block) \
+        + wl.qwz.phi * 5
+    free, _ = torch.cuda.mem_get_info()
+    if need > 0.8 * free:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB")
+    torch.cuda.empty_cache()
+    path = build_path(Z, wl, keep_grad=True)
+    path.run()
+    torch.cuda.synchronize()
+    check_qwz(path, wl, nsample=1)
+    check_qgz(path, wl, nsample=1)
+    del path
+    torch.cuda.empty_cache()

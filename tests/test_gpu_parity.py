@@ -1,0 +1,280 @@
+"""GPU parity, small cases: the CUDA path through the C ABI against the CPU
+oracle, element by element, on seeded inputs that span several warp units and
+CTA passes, ragged tails, every supported block size and both bit widths.
+
+Bar: codes, scales and the slice permutation bit-exact; reduced gradients
+within 1e-6 of the block's largest magnitude; Adam master/m/v within 1e-5
+relative; bf16 parameters within 1 ulp.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import workloads as W
+from gpu_helpers import (assert_bf16_ulp, assert_bytes_equal, assert_f32_bitexact,
+                         assert_grad_close, assert_rel_close, np_bytes, np_f32, u16, zpp)
+
+pytestmark = pytest.mark.gpu
+BLOCKS = [64, 128, 256, 512, 1024, 2048, 4096]
+RNG = np.random.default_rng(7)
+
+
+def special_values(n, bits, block, rng):
+    """fp32 values exercising every quantizer path: plain, all-zero blocks,
+    exact ties (x/s = k + 1/2), subnormal scales and single-spike blocks."""
+    qmax = (1 << (bits - 1)) - 1
+    x = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    nb = -(-n // block)
+    for b in range(nb):
+        lo, hi = b * block, min(n, (b + 1) * block)
+        kind = b % 6
+        e = 2.0 ** int(rng.integers(-20, 4))
+        if kind == 1:
+            x[lo:hi] = 0
+        elif kind == 2:      # ties: absmax qmax * 2^e, others (k + 1/2) 2^e
+            k = rng.integers(-qmax, qmax, size=hi - lo)
+            x[lo:hi] = (k + 0.5) * e
+            x[lo] = qmax * e
+        elif kind == 3:      # subnormal scale
+            x[lo:hi] = rng.integers(-1000, 1000, size=hi - lo) * 2.0 ** -142
+        elif kind == 4:      # one spike
+            x[lo:hi] = 0
+            x[lo + int(rng.integers(0, hi - lo))] = -3.0
+    return x
+
+
+def to_dev_bf16(x_f32, dev="cuda"):
+    return synth.u16_to_bf16(oracle.f32_to_bf16(x_f32)).to(dev)
+
+
+# ---- qwZ -------------------------------------------------------------------------------
+
+QWZ_SHAPES = [(1, 1), (1, 7), (1, 1000), (3, 4096), (2, 5000), (4, 3 * 4096 + 64),
+              (5, 777), (2, 9 * 1024 + 8), (1, 2 ** 17 + 40), (6, 2 * 4096 + 250)]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("block", BLOCKS)
+@pytest.mark.parametrize("nranks,shard", QWZ_SHAPES)
+def test_qwz_quant_dequant(bits, block, nranks, shard):
+    Z = zpp()
+    if bits == 4 and shard % 2:
+        shard += 1
+    n = nranks * shard
+    x = special_values(n, bits, block, RNG) if (block + shard) % 3 else \
+        (RNG.standard_t(3, n) * 1e-3).astype(np.float32)
+    xb = oracle.f32_to_bf16(x)
+    want_c, want_s = oracle.qwz_quant(xb, nranks, shard, block, bits)
+    want_y = oracle.qwz_dequant(want_c, want_s, nranks, shard, block, bits)
+
+    xd = synth.u16_to_bf16(xb).cuda()
+    codes = torch.full((want_c.size,), 0xAB, dtype=torch.uint8, device="cuda")
+    scales = torch.full((want_s.size,), float("nan"), dtype=torch.float32, device="cuda")
+    y = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    Z.zpp_qwz_quant(xd, nranks, shard, block, bits, codes, scales)
+    Z.zpp_qwz_dequant(codes, scales, nranks, shard, block, bits, y)
+    torch.cuda.synchronize()
+    assert_bytes_equal(np_bytes(codes), want_c, "codes")
+    assert_f32_bitexact(np_f32(scales), want_s, "scales")
+    assert_bytes_equal(u16(y), want_y, "dequant")
+
+
+def test_qwz_dequant_of_oracle_codes_and_empty_calls():
+    """Dequant alone on codes the oracle wrote; zero-sized calls are no-ops."""
+    Z = zpp()
+    nranks, shard, block = 3, 5000, 256
+    x = oracle.f32_to_bf16((RNG.standard_normal(nranks * shard) * 0.02).astype(np.float32))
+    c, s = oracle.qwz_quant(x, nranks, shard, block, 8)
+    y = torch.empty(nranks * shard, dtype=torch.bfloat16, device="cuda")
+    Z.zpp_qwz_dequant(torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda(), nranks, shard,
+                      block, 8, y)
+    torch.cuda.synchronize()
+    assert_bytes_equal(u16(y), oracle.qwz_dequant(c, s, nranks, shard, block, 8), "dequant")
+    e = torch.empty(0, device="cuda")
+    Z.zpp_qwz_quant(e.bfloat16(), 0, 100, 256, 8, e.byte(), e)
+    Z.zpp_qwz_quant(e.bfloat16(), 4, 0, 256, 4, e.byte(), e)
+    torch.cuda.synchronize()
+
+
+# ---- qgZ ----------------------------------------------------------------------------------
+
+TOPOS = [(1, 1), (1, 4), (2, 1), (2, 2), (2, 3), (3, 2), (4, 2), (2, 8), (1, 8), (4, 4)]
+
+
+def qgz_case(N, G, block, bits, slice_blocks, rng, special=False):
+    Nd = N * G
+    L = slice_blocks * block
+    bucket = Nd * L
+    if special:
+        x = special_values(Nd * bucket, bits, block, rng)
+    else:
+        x = (rng.standard_t(3, Nd * bucket) * 1e-3).astype(np.float32)
+    return Nd, L, bucket, oracle.f32_to_bf16(x)
+
+
+def run_gpu_chain(Z, gb, N, G, bucket, block, bits, adam=None, state=None, keep_grad=True):
+    Nd = N * G
+    L = bucket // Nd
+    g = synth.u16_to_bf16(gb).cuda()
+    c1 = torch.full((Nd * Z.zpp_codes_bytes(bucket, bits),), 0x5A, dtype=torch.uint8, device="cuda")
+    s1 = torch.full((Nd * (bucket // block),), float("nan"), device="cuda")
+    Z.zpp_qgz_reorder_quant(g, N, G, bucket, block, bits, c1, s1)
+    out = {"c1": c1, "s1": s1}
+    grad = torch.full((bucket,), float("nan"), device="cuda") if keep_grad else None
+    if N == 1:
+        Z.zpp_qgz_hop_reduce(1, c1, s1, N, G, bucket, block, bits, grad_out=grad, adam=adam,
+                             state=state)
+    else:
+        nl = N * L
+        c2 = torch.full((Nd * Z.zpp_codes_bytes(nl, bits),), 0x5A, dtype=torch.uint8, device="cuda")
+        s2 = torch.full((Nd * (nl // block),), float("nan"), device="cuda")
+        Z.zpp_qgz_hop_reduce(1, c1, s1, N, G, bucket, block, bits, codes_out=c2, scales_out=s2)
+        Z.zpp_qgz_hop_reduce(2, c2, s2, N, G, bucket, block, bits, grad_out=grad, adam=adam,
+                             state=state)
+        out.update(c2=c2, s2=s2)
+    torch.cuda.synchronize()
+    out["grad"] = grad
+    return out
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("block", [64, 256, 1024, 4096])
+@pytest.mark.parametrize("N,G", TOPOS)
+def test_qgz_chain(bits, block, N, G):
+    Z = zpp()
+    slice_blocks = {64: 19, 256: 5, 1024: 3, 4096: 1}[block]
+    Nd, L, bucket, gb = qgz_case(N, G, block, bits, slice_blocks, RNG, special=(N + G) % 2 == 0)
+    c1, s1 = oracle.qgz_reorder_quant(gb, N, G, bucket, block, bits)
+    got = run_gpu_chain(Z, gb, N, G, bucket, block, bits)
+    assert_bytes_equal(np_bytes(got["c1"]), c1, "one-shot codes")
+    assert_f32_bitexact(np_f32(got["s1"]), s1, "one-shot scales")
+    if N == 1:
+        want = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
+    else:
+        c2, s2 = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
+        assert_bytes_equal(np_bytes(got["c2"]), c2, "hop-1 codes")
+        assert_f32_bitexact(np_f32(got["s2"]), s2, "hop-1 scales")
+        want = oracle.qgz_hop2(c2, s2, N, G, bucket, block, bits)
+    g = np_f32(got["grad"])
+    assert_grad_close(g, want, block, "reduced gradient")
+    assert_f32_bitexact(g, want, "reduced gradient (bit-exact by construction)")
+
+
+def test_slice_permutation_through_the_message():
+    """The permutation is read back from the message itself: rank r's slice j,
+    filled with a constant that identifies (r, j), must be found at position
+    l'*N + n' with j = n'*G + l'."""
+    Z = zpp()
+    N, G, block, bits = 3, 4, 64, 8
+    Nd = N * G
+    L, bucket = 2 * block, Nd * 2 * block
+    x = np.zeros((Nd, Nd, L), np.float32)
+    for r in range(Nd):
+        for j in range(Nd):
+            x[r, j, :] = r * 16 + j + 1        # <= 188: exact in bf16
+            x[r, j, 0] = 1000.0                # same absmax everywhere
+    gb = oracle.f32_to_bf16(x.reshape(-1))
+    got = run_gpu_chain(Z, gb, N, G, bucket, block, bits)
+    q = np_bytes(got["c1"]).view(np.int8).reshape(Nd, Nd, L)
+    perm = Z.zpp_qgz_slice_perm(N, G)
+    for r in range(Nd):
+        for p in range(Nd):
+            j = perm[p]
+            want = np.rint(np.float32(r * 16 + j + 1) / (np.float32(1000.0) / np.float32(127)))
+            assert q[r, p, 1] == want
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("N,G", [(1, 8), (2, 2), (2, 8), (3, 2)])
+def test_final_hop_fused_adam(bits, N, G):
+    Z = zpp()
+    block = 256
+    Nd, L, bucket, gb = qgz_case(N, G, block, bits, 6, RNG)
+    want_g = oracle.qgz_reduce_scatter(gb, N, G, bucket, block, bits)
+    p0 = (RNG.standard_normal(bucket) * 0.02).astype(np.float32)
+    m0 = (RNG.standard_normal(bucket) * 1e-4).astype(np.float32)
+    v0 = np.abs(RNG.standard_normal(bucket) * 1e-6).astype(np.float32)
+    hp = (1e-4, 0.9, 0.999, 1e-8, 3)
+    wp, wm, wv, wb = oracle.adam_step(want_g, p0, m0, v0, *hp)
+    master, m, v = (torch.from_numpy(a.copy()).cuda() for a in (p0, m0, v0))
+    param = torch.empty(bucket, dtype=torch.bfloat16, device="cuda")
+    got = run_gpu_chain(Z, gb, N, G, bucket, block, bits, adam=hp, state=(master, m, v, param))
+    assert_f32_bitexact(np_f32(got["grad"]), want_g, "gradient")
+    assert_rel_close(np_f32(master), wp, 1e-5, "master")
+    assert_rel_close(np_f32(m), wm, 1e-5, "m")
+    assert_rel_close(np_f32(v), wv, 1e-5, "v")
+    assert_bf16_ulp(u16(param), wb, "param")
+    # the kernel evaluates the same IEEE operations in the same order
+    assert_f32_bitexact(np_f32(master), wp, "master (bit-exact)")
+
+
+def test_fused_adam_without_grad_out_and_no_param():
+    Z = zpp()
+    N, G, block, bits = 2, 4, 512, 4
+    Nd, L, bucket, gb = qgz_case(N, G, block, bits, 2, RNG)
+    want_g = oracle.qgz_reduce_scatter(gb, N, G, bucket, block, bits)
+    z = np.zeros(bucket, np.float32)
+    p0 = (RNG.standard_normal(bucket) * 0.02).astype(np.float32)
+    wp, wm, wv, _ = oracle.adam_step(want_g, p0, z, z, 1e-4, 0.9, 0.999, 1e-8, 1)
+    master = torch.from_numpy(p0.copy()).cuda()
+    m = torch.zeros(bucket, device="cuda")
+    v = torch.zeros(bucket, device="cuda")
+    run_gpu_chain(Z, gb, N, G, bucket, block, bits, adam=(1e-4, 0.9, 0.999, 1e-8, 1),
+                  state=(master, m, v, None), keep_grad=False)
+    assert_f32_bitexact(np_f32(master), wp, "master")
+    assert_f32_bitexact(np_f32(m), wm, "m")
+    assert_f32_bitexact(np_f32(v), wv, "v")
+
+
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 511, 512, 1000, 123457])
+@pytest.mark.parametrize("t", [1, 2, 50])
+def test_standalone_adam(n, t):
+    Z = zpp()
+    g = (RNG.standard_normal(n) * 1e-3).astype(np.float32)
+    p0 = (RNG.standard_normal(n) * 0.02).astype(np.float32)
+    m0 = (RNG.standard_normal(n) * 1e-4).astype(np.float32) if t > 1 else np.zeros(n, np.float32)
+    v0 = np.abs(RNG.standard_normal(n) * 1e-6).astype(np.float32) if t > 1 else np.zeros(n, np.float32)
+    hp = (3e-4, 0.9, 0.95, 1e-6, t)
+    wp, wm, wv, wb = oracle.adam_step(g, p0, m0, v0, *hp)
+    master, m, v = (torch.from_numpy(a.copy()).cuda() for a in (p0, m0, v0))
+    param = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    Z.zpp_shard_adam_step(torch.from_numpy(g).cuda(), n, hp, (master, m, v, param))
+    torch.cuda.synchronize()
+    assert_rel_close(np_f32(master), wp, 1e-5, "master")
+    assert_rel_close(np_f32(m), wm, 1e-5, "m")
+    assert_rel_close(np_f32(v), wv, 1e-5, "v")
+    assert_bf16_ulp(u16(param), wb, "param")
+    assert_f32_bitexact(np_f32(master), wp, "master (bit-exact)")
+
+
+def test_tiny_workload_end_to_end():
+    """The tiny workload through CodecPath (the sequence the bench times)."""
+    Z = zpp()
+    from gradient_comm_codecs_gb300 import AdamSpec, CodecPath, QgzSpec, QwzSpec
+    wl = W.TINY
+    q, g = wl.qwz, wl.qgz
+    path = CodecPath(QwzSpec(q.nranks, q.shard, q.block, q.bits),
+                     QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits),
+                     AdamSpec(), device="cuda", keep_grad=True)
+    w = synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, q.phi)
+    path.w.copy_(w)
+    from gpu_helpers import grads_for
+    grads = grads_for(g, wl.seed)
+    path.grads.copy_(grads)
+    master0 = synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, g.bucket).float()
+    path.master.copy_(master0)
+    path.run()
+    torch.cuda.synchronize()
+    wb = u16(w)
+    c, s = oracle.qwz_quant(wb, q.nranks, q.shard, q.block, q.bits)
+    assert_bytes_equal(u16(path.w_full), oracle.qwz_dequant(c, s, q.nranks, q.shard, q.block,
+                                                            q.bits), "qwZ all-gather")
+    gref = oracle.qgz_reduce_scatter(u16(grads), g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+    assert_f32_bitexact(np_f32(path.grad_out), gref, "reduced gradient")
+    z = np.zeros(g.bucket, np.float32)
+    wp, wm, wv, wpb = oracle.adam_step(gref, master0.numpy(), z, z, wl.adam.lr, wl.adam.beta1,
+                                       wl.adam.beta2, wl.adam.eps, wl.adam.step)
+    assert_rel_close(np_f32(path.master), wp, 1e-5, "master")
+    assert_bf16_ulp(u16(path.param), wpb, "param")
