@@ -496,10 +496,14 @@ def main():
     ap.add_argument("--config", default="llama", choices=["tiny", "llama", "two_hop", "7b"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--scale", type=int, default=1,
+                    help="divide the workload's shard and bucket by this (small profiling cases)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     from synth import workloads as W
     wl = W.WORKLOADS[args.config]
+    if args.scale > 1:
+        wl = W.scaled(wl, args.scale)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -139,3 +139,17 @@ def sweep_points():
                                 bits=bits),
                         fused_adam=False, seed=i)
                     i += 1
+
+
+def scaled(wl: Workload, factor: int) -> Workload:
+    """The same workload with every shard and bucket divided by `factor`
+    (rounded down to whole blocks per slice): a smaller instance for profiling."""
+    import dataclasses
+    q, g = wl.qwz, wl.qgz
+    if q is not None:
+        shard = max(q.block, (q.shard // factor) // q.block * q.block)
+        q = dataclasses.replace(q, shard=shard, calls=1, tail_shard=0)
+    if g is not None:
+        unit = g.nd * g.block
+        g = dataclasses.replace(g, bucket=max(unit, (g.bucket // factor) // unit * unit))
+    return dataclasses.replace(wl, name=f"{wl.name} / {factor}", qwz=q, qgz=g)

@@ -67,10 +67,17 @@ def build_path(Z, wl: W.Workload, keep_grad=True):
 
 
 def check_qwz(path, wl, nsample=3):
+    """Sampled blocks of every call's dequantized output; codes and scales of
+    the last call of each shard size (earlier calls of the same size reuse
+    that call's code buffer, as a streamed long tensor does)."""
     q = wl.qwz
     B, bits = q.block, q.bits
-    off = 0
-    for call, s in enumerate(path.qwz.call_shards()):
+    shards = path.qwz.call_shards()
+    last_of = {s: i for i, s in enumerate(shards)}
+    calls = sorted({0, len(shards) - 1, len(shards) // 2} | set(last_of.values()))
+    offs = np.concatenate([[0], np.cumsum([q.nranks * s for s in shards])])
+    for call in calls:
+        s, off = shards[call], int(offs[call])
         i = path._codes_of[s]
         codes, scales = path.w_codes[i], path.w_scales[i]
         nb = -(-s // B)
@@ -82,13 +89,13 @@ def check_qwz(path, wl, nsample=3):
                 x = synth.bf16_to_u16(synth.at(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, gidx))
                 wc, ws = oracle.qwz_quant(x, 1, n, B, bits)
                 wy = oracle.qwz_dequant(wc, ws, 1, n, B, bits)
+                assert_bytes_equal(gather_u16(path.w_full, gidx), wy, f"qwZ dequant {call}/{r}/{b}")
+                if last_of[s] != call:
+                    continue
                 got_c = gather_bytes(codes, [r * cb + (b * B * bits) // 8], wc.size)
                 assert_bytes_equal(got_c, wc, f"qwZ codes call {call} rank {r} block {b}")
                 got_s = gather_f32(scales, [r * nb + b])
                 assert_f32_bitexact(got_s, ws, f"qwZ scale call {call} rank {r} block {b}")
-                assert_bytes_equal(gather_u16(path.w_full, gidx), wy, f"qwZ dequant {call}/{r}/{b}")
-        # only a few calls of a long tensor: first, last, one in between
-        off += q.nranks * s
 
 
 def check_qgz(path, wl, nsample=2):
@@ -199,7 +206,7 @@ def test_7b_standalone_adam_full_size():
     assert_bf16_ulp(gather_u16(param, idx), wb, "param")
 
 
-SWEEP_SAMPLE = [0, 7, 23, 30, 47, 53, 70, 95, 101, 118, 131, 141]
+SWEEP_SAMPLE = [0, 7, 20, 30, 47, 50, 70, 95, 101, 118, 131, 141]
 
 
 @pytest.mark.parametrize("index", SWEEP_SAMPLE)
