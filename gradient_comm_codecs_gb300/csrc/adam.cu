@@ -31,16 +31,26 @@ __global__ void __launch_bounds__(kThreads) adam_kernel(const AdamArgs a) {
   const int64_t units = (a.n + kAdamUnit - 1) / kAdamUnit;
   for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units;
        u += (int64_t)gridDim.x * kWarps) {
+    const int64_t base = u * kAdamUnit + lane * 8;
+    if (base + (kAdamRows - 1) * 256 + 8 <= a.n) {
+      float g[kAdamRows][8];
+      AdamVec s[kAdamRows];
 #pragma unroll
-    for (int k = 0; k < kAdamRows; ++k) {
-      const int64_t idx = u * kAdamUnit + (k * 32 + lane) * 8;
-      if (idx + 8 <= a.n) {
-        const float4* gp = reinterpret_cast<const float4*>(a.g + idx);
+      for (int k = 0; k < kAdamRows; ++k) {
+        const float4* gp = reinterpret_cast<const float4*>(a.g + base + k * 256);
         const float4 g0 = __ldcs(gp), g1 = __ldcs(gp + 1);
-        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        adam_update8(g, idx, a.master, a.m, a.v, a.param, a.ac);
-      } else {
-        for (int64_t i = idx; i < a.n; ++i) {
+        g[k][0] = g0.x; g[k][1] = g0.y; g[k][2] = g0.z; g[k][3] = g0.w;
+        g[k][4] = g1.x; g[k][5] = g1.y; g[k][6] = g1.z; g[k][7] = g1.w;
+        s[k] = adam_load8(base + k * 256, a.master, a.m, a.v);
+      }
+#pragma unroll
+      for (int k = 0; k < kAdamRows; ++k)
+        adam_apply8(g[k], s[k], base + k * 256, a.master, a.m, a.v, a.param, a.ac);
+    } else {
+#pragma unroll
+      for (int k = 0; k < kAdamRows; ++k) {
+        const int64_t idx = base + k * 256;
+        for (int64_t i = idx; i < idx + 8 && i < a.n; ++i) {
           float p = a.master[i], m = a.m[i], v = a.v[i];
           adam_update(a.g[i], p, m, v, a.ac);
           a.master[i] = p;

@@ -10,6 +10,11 @@
 // chunk straight out of every peer's message in HBM.  One pass per hop fuses
 // dequantize -> fp32 sum in rank order -> requantize (hop 1 of a two-hop
 // topology) or -> x (1/N_d) -> fp32 gradient and/or the Adam step (final hop).
+//
+// Memory-level parallelism: the sources are read in chunks whose loads are
+// all issued before the chunk is summed, and the next chunk's loads are in
+// flight while the current one is summed (two register buffers); in the Adam
+// mode the optimizer state of the unit is loaded before the sum starts.
 #include "zpp_device.cuh"
 #include "zpp_launch.h"
 
@@ -24,12 +29,10 @@ struct HopArgs {
   int32_t hop, N, G;
   int64_t R;               // output elements per destination rank
   int64_t units_per_row, total_units;
-  int32_t block;
   uint8_t* codes_out;      // requant
   float* scales_out;
   float* grad_out;         // final
   float inv_nd;
-  int32_t adam;
   AdamConsts ac;
   float* master;
   float* m;
@@ -37,128 +40,188 @@ struct HopArgs {
   uint16_t* param;
 };
 
-constexpr int kSrcChunk = 4;  // sources whose loads are in flight together
+enum { kRequant = 0, kFinal = 1, kFinalAdam = 2 };
 
-// MODE 0: hop 1 of a two-hop topology (requantize); MODE 1: final hop.
-template <int BITS, int MODE>
+template <int MODE>
+constexpr int hop_rows() { return MODE == kFinalAdam ? 2 : 4; }
+
+template <int BITS, int MODE, int LOGB>
+struct HopCfg {
+  static constexpr int K = hop_rows<MODE>();
+  using G = Geo<LOGB, K>;
+  static constexpr int WPB = MODE == kRequant ? G::WPB : 1;   // final hops need no block absmax
+  static constexpr int U = WPB * G::kWarpElems;
+  static constexpr int SCH = BITS == 4 ? 4 : 2;                // sources per load chunk
+};
+
+template <int BITS, int K, int NSC, int SCH>
+struct Chunk {
+  typename CodeVec<BITS>::T c[SCH][K];
+  float s[SCH][NSC];
+};
+
+template <int BITS, int MODE, int LOGB>
 __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
-  __shared__ float red[2][kWarps];
+  using C = HopCfg<BITS, MODE, LOGB>;
+  using G = typename C::G;
+  constexpr int K = C::K, WPB = C::WPB, SCH = C::SCH, NSC = G::NSC, RPB = G::RPB;
+  constexpr int QMAX = (1 << (BITS - 1)) - 1;
+  constexpr int GPC = kWarps / WPB;
   using CW = typename CodeVec<BITS>::T;
-  constexpr int qmax = (1 << (BITS - 1)) - 1;
+  using CH = Chunk<BITS, K, NSC, SCH>;
+  __shared__ float red[2][kWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = a.block;
-  const int wpb = (MODE == 0 && B > kWarpElems) ? B / kWarpElems : 1;
-  const int gpc = kWarps / wpb;
-  const int gid = warp / wpb, wsub = warp - gid * wpb;
-  const int64_t U = (int64_t)wpb * kWarpElems;
+  const int gid = warp / WPB, wsub = warp - gid * WPB;
+
+  int64_t u, uend;
+  unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
+  if (u >= uend) return;
+  int64_t d = u / a.units_per_row;
+  int64_t t = u - d * a.units_per_row;
+  int32_t dn = (int32_t)(d / a.G), dl = (int32_t)(d - (int64_t)dn * a.G);
   int parity = 0;
 
-  for (int64_t u = (int64_t)blockIdx.x * gpc + gid; u < a.total_units;
-       u += (int64_t)gridDim.x * gpc, parity ^= 1) {
-    const int64_t d = u / a.units_per_row;
-    const int64_t t = u - d * a.units_per_row;
-    const int32_t dn = (int32_t)(d / a.G), dl = (int32_t)(d - (int64_t)dn * a.G);
+  for (; u < uend; ++u, parity ^= 1) {
     // hop 1: sources n*G + g, chunk l;  hop 2: sources n'*G + l, slot n
     const int64_t src0 = a.hop == 1 ? (int64_t)dn * a.G : dl;
     const int64_t sstride = a.hop == 1 ? 1 : a.G;
     const int64_t in_off = (a.hop == 1 ? (int64_t)dl : (int64_t)dn) * a.R;
-    const int64_t e_warp = t * U + (int64_t)wsub * kWarpElems;
+    const int64_t e_warp = t * C::U + (int64_t)wsub * G::kWarpElems;
     const int64_t valid = a.R - e_warp;  // a multiple of 64 when positive
+    const int64_t obase = d * a.R + e_warp;
+    bool on[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) on[k] = (int64_t)(k * 256 + lane * 8) < valid;
 
-    bool on[kRows];
+    AdamVec st[MODE == kFinalAdam ? K : 1];
+    if constexpr (MODE == kFinalAdam) {
 #pragma unroll
-    for (int k = 0; k < kRows; ++k) on[k] = (int64_t)(k * 32 + lane) * 8 < valid;
+      for (int k = 0; k < K; ++k)
+        if (on[k]) st[k] = adam_load8(obase + k * 256 + lane * 8, a.master, a.m, a.v);
+    }
 
-    float acc[kRows][8];
+    auto load = [&](CH& ch, int s0) {
 #pragma unroll
-    for (int k = 0; k < kRows; ++k)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[k][i] = 0.0f;
-
-    for (int s0 = 0; s0 < a.S; s0 += kSrcChunk) {
-      CW cw[kSrcChunk][kRows];
-      float sc[kSrcChunk][kRows];
-#pragma unroll
-      for (int j = 0; j < kSrcChunk; ++j) {
+      for (int j = 0; j < SCH; ++j) {
         const int s = s0 + j;
         const int64_t pb = (src0 + (int64_t)s * sstride) * a.in_rank_elems + in_off + e_warp;
 #pragma unroll
-        for (int k = 0; k < kRows; ++k) {
-          const int64_t pos = pb + (k * 32 + lane) * 8;
-          if (s < a.S && on[k]) {
-            cw[j][k] = __ldcs(reinterpret_cast<const CW*>(a.codes_in + (pos * BITS) / 8));
-            sc[j][k] = __ldg(a.scales_in + pos / B);
-          } else {
-            cw[j][k] = CW{};
-            sc[j][k] = 0.0f;
-          }
+        for (int k = 0; k < K; ++k) {
+          const int64_t pos = pb + k * 256 + lane * 8;
+          ch.c[j][k] = (s < a.S && on[k])
+                           ? __ldcs(reinterpret_cast<const CW*>(a.codes_in + ((pos * BITS) >> 3)))
+                           : CW{};
+        }
+#pragma unroll
+        for (int i = 0; i < NSC; ++i) {
+          const int64_t pos = pb + i * RPB * 256 + lane * 8;
+          ch.s[j][i] = (s < a.S && on[i * RPB]) ? __ldg(a.scales_in + (pos >> LOGB)) : 0.0f;
         }
       }
+    };
+    float acc[K][8];
 #pragma unroll
-      for (int j = 0; j < kSrcChunk; ++j) {
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[k][i] = 0.0f;
+    auto sum = [&](const CH& ch, int s0) {
+#pragma unroll
+      for (int j = 0; j < SCH; ++j) {
         if (s0 + j >= a.S) break;
 #pragma unroll
-        for (int k = 0; k < kRows; ++k) {
+        for (int k = 0; k < K; ++k) {
           float q[8];
-          decode8<BITS>(cw[j][k], q);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[k][i] = __fadd_rn(acc[k][i], __fmul_rn(q[i], sc[j][k]));
+          decode8<BITS>(ch.c[j][k], q);
+          accumulate8(acc[k], q, ch.s[j][k / RPB]);
         }
       }
+    };
+
+    CH ca, cb;
+    load(ca, 0);
+    for (int c = 0; c < a.S; c += 2 * SCH) {
+      if (c + SCH < a.S) load(cb, c + SCH);
+      sum(ca, c);
+      if (c + SCH >= a.S) break;
+      if (c + 2 * SCH < a.S) load(ca, c + 2 * SCH);
+      sum(cb, c + SCH);
     }
 
-    const int64_t obase = d * a.R + e_warp;  // output element of this warp's first vector
-    if constexpr (MODE == 0) {
-      float am[kRows];
+    if constexpr (MODE == kRequant) {
+      float am[K];
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
+      for (int k = 0; k < K; ++k) {
         float m = fabsf(acc[k][0]);
 #pragma unroll
         for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(acc[k][i]));
         am[k] = m;
       }
-      warp_block_absmax(am, B);
-      if (wpb > 1) {
-        const float m = group_absmax(am[0], red, parity, warp, gid, wpb, lane);
+      warp_block_absmax<G>(am);
+      if constexpr (WPB > 1) {
+        const float m = group_absmax<WPB>(am[0], red, parity, warp, gid, lane);
 #pragma unroll
-        for (int k = 0; k < kRows; ++k) am[k] = m;
+        for (int k = 0; k < K; ++k) am[k] = m;
       }
+      Scale sc[NSC];
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
+      for (int i = 0; i < NSC; ++i) sc[i] = make_scale(am[i * RPB], (float)QMAX);
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
         if (!on[k]) continue;
-        const int e = (k * 32 + lane) * 8;
-        const Scale scl = make_scale(am[k], (float)qmax);
+        const int e = k * 256 + lane * 8;
         uint32_t c[8];
-        quantize8(acc[k], scl, qmax, c);
-        *reinterpret_cast<CW*>(a.codes_out + ((obase + e) * BITS) / 8) = pack8<BITS>(c);
-        if (((e_warp + e) & (B - 1)) == 0) a.scales_out[(obase + e) / B] = scl.s;
+        quantize8<QMAX>(acc[k], sc[k / RPB], c);
+        *reinterpret_cast<CW*>(a.codes_out + (((obase + e) * BITS) >> 3)) = pack8<BITS>(c);
+        if (((e_warp + e) & (G::B - 1)) == 0) a.scales_out[(obase + e) >> LOGB] = sc[k / RPB].s;
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
+      for (int k = 0; k < K; ++k) {
         if (!on[k]) continue;
-        const int64_t idx = obase + (k * 32 + lane) * 8;
+        const int64_t idx = obase + k * 256 + lane * 8;
         float g[8];
+        const float2 inv = make_float2(a.inv_nd, a.inv_nd);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) g[i] = __fmul_rn(acc[k][i], a.inv_nd);
+        for (int i = 0; i < 8; i += 2) {
+          const float2 v = mul2(make_float2(acc[k][i], acc[k][i + 1]), inv);
+          g[i] = v.x;
+          g[i + 1] = v.y;
+        }
         if (a.grad_out) {
           float4* go = reinterpret_cast<float4*>(a.grad_out + idx);
           __stcs(go, make_float4(g[0], g[1], g[2], g[3]));
           __stcs(go + 1, make_float4(g[4], g[5], g[6], g[7]));
         }
-        if (a.adam) adam_update8(g, idx, a.master, a.m, a.v, a.param, a.ac);
+        if constexpr (MODE == kFinalAdam)
+          adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac);
+      }
+    }
+
+    if (++t == a.units_per_row) {
+      t = 0;
+      ++d;
+      if (++dl == a.G) {
+        dl = 0;
+        ++dn;
       }
     }
   }
 }
 
 template <int BITS, int MODE>
-cudaError_t run_hop(const HopArgs& a, cudaStream_t st) {
-  const void* k = reinterpret_cast<const void*>(&hop_kernel<BITS, MODE>);
-  const int wpb = (MODE == 0 && a.block > kWarpElems) ? a.block / kWarpElems : 1;
-  const int gpc = kWarps / wpb;
-  hop_kernel<BITS, MODE><<<grid_for(k, (a.total_units + gpc - 1) / gpc), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
+  return dispatch_logb(block, [&](auto lb) -> cudaError_t {
+    constexpr int LOGB = decltype(lb)::value;
+    using C = HopCfg<BITS, MODE, LOGB>;
+    HopArgs a = a0;
+    a.units_per_row = (a.R + C::U - 1) / C::U;
+    a.total_units = (int64_t)a.N * a.G * a.units_per_row;
+    const void* k = reinterpret_cast<const void*>(&hop_kernel<BITS, MODE, LOGB>);
+    const int64_t groups = kWarps / C::WPB;
+    hop_kernel<BITS, MODE, LOGB>
+        <<<grid_for(k, (a.total_units + groups - 1) / groups), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+  });
 }
 
 }  // namespace
@@ -176,23 +239,20 @@ cudaError_t launch_hop_reduce(const HopLaunch& h, cudaStream_t st) {
   a.S = h.hop == 1 ? h.G : h.N;
   a.in_rank_elems = h.hop == 1 ? h.bucket : (int64_t)h.N * L;
   a.R = (h.hop == 1 && h.N > 1) ? (int64_t)h.N * L : L;
-  const int64_t U = (!final_hop && h.block > kWarpElems) ? h.block : kWarpElems;
-  a.units_per_row = (a.R + U - 1) / U;
-  a.total_units = (int64_t)nd * a.units_per_row;
-  a.block = h.block;
   a.codes_out = static_cast<uint8_t*>(h.codes_out);
   a.scales_out = h.scales_out;
   a.grad_out = h.grad_out;
   a.inv_nd = h.inv_nd;
-  a.adam = h.adam ? 1 : 0;
   a.ac = AdamConsts{h.ac.lr, h.ac.beta1, h.ac.beta2, h.ac.eps,
                     h.ac.omb1, h.ac.omb2, h.ac.bc1, h.ac.bc2};
   a.master = h.master;
   a.m = h.m;
   a.v = h.v;
   a.param = h.param;
-  if (final_hop) return h.bits == 8 ? run_hop<8, 1>(a, st) : run_hop<4, 1>(a, st);
-  return h.bits == 8 ? run_hop<8, 0>(a, st) : run_hop<4, 0>(a, st);
+  const int b = h.block;
+  if (!final_hop) return h.bits == 8 ? run_hop<8, kRequant>(a, b, st) : run_hop<4, kRequant>(a, b, st);
+  if (h.adam) return h.bits == 8 ? run_hop<8, kFinalAdam>(a, b, st) : run_hop<4, kFinalAdam>(a, b, st);
+  return h.bits == 8 ? run_hop<8, kFinal>(a, b, st) : run_hop<4, kFinal>(a, b, st);
 }
 
 }  // namespace zpp

@@ -15,6 +15,8 @@
 namespace zpp {
 namespace {
 
+constexpr int kQRows = 4;  // rows of 256 elements per warp slab
+
 struct QuantArgs {
   const uint16_t* x;
   uint8_t* codes;
@@ -25,64 +27,68 @@ struct QuantArgs {
   int64_t row_blocks;     // qwZ: scales per shard
   int64_t bucket;         // qgZ: elements per rank
   int32_t nd, N, G;       // qgZ topology
-  int32_t block;
 };
 
-// One row = one contiguous run that is quantized in blocks restarting at the
-// row start: a qwZ shard, or one slice (rank r, slice j) of a qgZ bucket whose
-// codes go to slice position p = (j % G) * N + j / G of rank r's message.
-template <int BITS, bool REORDER>
+// One row = one contiguous run quantized in blocks restarting at the row
+// start: a qwZ shard, or slice j of rank r's qgZ bucket, whose codes go to
+// slice position p = l'*N + n' (j = n'*G + l') of rank r's message.
+template <int BITS, bool REORDER, int LOGB>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
-  __shared__ float red[2][kWarps];
+  using G = Geo<LOGB, kQRows>;
+  constexpr int K = kQRows;
+  constexpr int QMAX = (1 << (BITS - 1)) - 1;
+  constexpr int GPC = kWarps / G::WPB;  // warp groups per CTA
   using CW = typename CodeVec<BITS>::T;
-  constexpr int qmax = (1 << (BITS - 1)) - 1;
+  __shared__ float red[2][kWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = a.block;
-  const int wpb = B > kWarpElems ? B / kWarpElems : 1;  // warps per unit
-  const int gpc = kWarps / wpb;                         // units per CTA pass
-  const int gid = warp / wpb, wsub = warp - gid * wpb;
-  const int64_t U = (int64_t)wpb * kWarpElems;
+  const int gid = warp / G::WPB, wsub = warp - gid * G::WPB;
+
+  int64_t u, uend;
+  unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
+  if (u >= uend) return;  // the whole group shares the range
+  int64_t row = u / a.units_per_row;
+  int64_t t = u - row * a.units_per_row;
+  int32_t r = 0, j = 0, np = 0, lp = 0;  // qgZ: row = r*nd + j, j = np*G + lp
+  if constexpr (REORDER) {
+    r = (int32_t)(row / a.nd);
+    j = (int32_t)(row - (int64_t)r * a.nd);
+    np = j / a.G;
+    lp = j - np * a.G;
+  }
   int parity = 0;
 
-  for (int64_t u = (int64_t)blockIdx.x * gpc + gid; u < a.total_units;
-       u += (int64_t)gridDim.x * gpc, parity ^= 1) {
-    const int64_t row = u / a.units_per_row;
-    const int64_t t = u - row * a.units_per_row;
-    int64_t src_base, dst_base, scale_base;
+  for (; u < uend; ++u, parity ^= 1) {
+    int64_t dst_base, scale_base;
+    const int64_t src_base = row * a.row_len;
     if constexpr (REORDER) {
-      const int32_t r = (int32_t)(row / a.nd);
-      const int32_t j = (int32_t)(row - (int64_t)r * a.nd);
-      const int32_t p = (j % a.G) * a.N + j / a.G;
-      src_base = (int64_t)r * a.bucket + (int64_t)j * a.row_len;
-      dst_base = (int64_t)r * a.bucket + (int64_t)p * a.row_len;
-      scale_base = dst_base / B;
+      dst_base = (int64_t)r * a.bucket + ((int64_t)lp * a.N + np) * a.row_len;
+      scale_base = dst_base >> LOGB;
     } else {
-      src_base = row * a.row_len;
       dst_base = src_base;
       scale_base = row * a.row_blocks;
     }
-    const int64_t e_warp = t * U + (int64_t)wsub * kWarpElems;  // first element (row-relative)
+    const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;  // row-relative
     const int64_t valid = a.row_len - e_warp;
     const bool aligned = ((src_base | dst_base) & 7) == 0;
-    const bool full = aligned && valid >= kWarpElems;
+    const bool full = aligned && valid >= G::kWarpElems;
     const uint16_t* xw = a.x + src_base + e_warp;
 
-    float x[kRows][8];
-    int nv[kRows];
+    float x[K][8];
+    int nv[K];
     if (full) {
-      uint4 w[kRows];
+      uint4 w[K];
 #pragma unroll
-      for (int k = 0; k < kRows; ++k)
-        w[k] = __ldcs(reinterpret_cast<const uint4*>(xw + (k * 32 + lane) * 8));
+      for (int k = 0; k < K; ++k)
+        w[k] = __ldcs(reinterpret_cast<const uint4*>(xw + k * 256 + lane * 8));
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
+      for (int k = 0; k < K; ++k) {
         unpack_bf16x8(w[k], x[k]);
         nv[k] = 8;
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const int e = (k * 32 + lane) * 8;
+      for (int k = 0; k < K; ++k) {
+        const int e = k * 256 + lane * 8;
         const int64_t rem = valid - e;
         nv[k] = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
 #pragma unroll
@@ -91,39 +97,63 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
       }
     }
 
-    float am[kRows];
+    float am[K];
 #pragma unroll
-    for (int k = 0; k < kRows; ++k) {
+    for (int k = 0; k < K; ++k) {
       float m = fabsf(x[k][0]);
 #pragma unroll
       for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(x[k][i]));
       am[k] = m;
     }
-    warp_block_absmax(am, B);
-    if (wpb > 1) {
-      const float m = group_absmax(am[0], red, parity, warp, gid, wpb, lane);
+    warp_block_absmax<G>(am);
+    if constexpr (G::WPB > 1) {
+      const float m = group_absmax<G::WPB>(am[0], red, parity, warp, gid, lane);
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) am[k] = m;
+      for (int k = 0; k < K; ++k) am[k] = m;
     }
-
-    uint8_t* cw = a.codes + ((dst_base + e_warp) * BITS) / 8;
+    Scale sc[G::NSC];
 #pragma unroll
-    for (int k = 0; k < kRows; ++k) {
+    for (int i = 0; i < G::NSC; ++i) sc[i] = make_scale(am[i * G::RPB], (float)QMAX);
+
+    uint8_t* cw = a.codes + (((dst_base + e_warp) * BITS) >> 3);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
       if (nv[k] == 0) continue;
-      const int e = (k * 32 + lane) * 8;
-      const Scale sc = make_scale(am[k], (float)qmax);
+      const int e = k * 256 + lane * 8;
       uint32_t c[8];
-      quantize8(x[k], sc, qmax, c);
+      quantize8<QMAX>(x[k], sc[k / G::RPB], c);
       const CW w = pack8<BITS>(c);
-      uint8_t* dst = cw + (e * BITS) / 8;
+      uint8_t* dst = cw + ((e * BITS) >> 3);
       if (nv[k] == 8 && aligned) {
         *reinterpret_cast<CW*>(dst) = w;
       } else {
-        const int nbytes = (nv[k] * BITS + 7) / 8;
-        const uint8_t* wb = reinterpret_cast<const uint8_t*>(&w);
-        for (int i = 0; i < nbytes; ++i) dst[i] = wb[i];
+        uint32_t lo, hi = 0;
+        if constexpr (BITS == 8) {
+          lo = w.x;
+          hi = w.y;
+        } else {
+          lo = w;
+        }
+        const int nbytes = (nv[k] * BITS + 7) >> 3;
+        for (int i = 0; i < nbytes; ++i) dst[i] = (uint8_t)((i < 4 ? lo >> (8 * i) : hi >> (8 * (i - 4))) & 0xFF);
       }
-      if (((e_warp + e) & (B - 1)) == 0) a.scales[scale_base + (e_warp + e) / B] = sc.s;
+      if (((e_warp + e) & (G::B - 1)) == 0) a.scales[scale_base + ((e_warp + e) >> LOGB)] = sc[k / G::RPB].s;
+    }
+
+    if (++t == a.units_per_row) {
+      t = 0;
+      ++row;
+      if constexpr (REORDER) {
+        ++j;
+        if (++lp == a.G) {
+          lp = 0;
+          ++np;
+        }
+        if (j == a.nd) {
+          j = np = lp = 0;
+          ++r;
+        }
+      }
     }
   }
 }
@@ -134,88 +164,106 @@ struct DequantArgs {
   uint16_t* y;
   int64_t total_units, units_per_row;
   int64_t row_len, row_blocks;
-  int32_t block;
 };
 
 // y = bf16_rn((float)q * s) for every element of every shard.
-template <int BITS>
+template <int BITS, int LOGB>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) {
+  using G = Geo<LOGB, kQRows>;
+  constexpr int K = kQRows;
+  constexpr int WE = G::kWarpElems;
   using CW = typename CodeVec<BITS>::T;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < a.total_units;
-       u += (int64_t)gridDim.x * kWarps) {
-    const int64_t row = u / a.units_per_row;
-    const int64_t t = u - row * a.units_per_row;
+  int64_t u, uend;
+  unit_range(a.total_units, (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps, u, uend);
+  if (u >= uend) return;
+  int64_t row = u / a.units_per_row;
+  int64_t t = u - row * a.units_per_row;
+  for (; u < uend; ++u) {
     const int64_t base = row * a.row_len;
-    const int64_t e_warp = t * kWarpElems;
+    const int64_t e_warp = t * WE;
     const int64_t valid = a.row_len - e_warp;
-    const bool aligned = (base & 7) == 0;
-    const bool full = aligned && valid >= kWarpElems;
-    const uint8_t* cw = a.codes + ((base + e_warp) * BITS) / 8;
+    const bool full = ((base & 7) == 0) && valid >= WE;
+    const uint8_t* cw = a.codes + (((base + e_warp) * BITS) >> 3);
     const float* sw = a.scales + row * a.row_blocks;
     uint16_t* yw = a.y + base + e_warp;
     if (full) {
-      CW w[kRows];
-      float s[kRows];
+      CW w[K];
+      float s[K];
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const int e = (k * 32 + lane) * 8;
-        w[k] = __ldcs(reinterpret_cast<const CW*>(cw + (e * BITS) / 8));
-        s[k] = __ldg(sw + (e_warp + e) / a.block);
+      for (int k = 0; k < K; ++k) {
+        const int e = k * 256 + lane * 8;
+        w[k] = __ldcs(reinterpret_cast<const CW*>(cw + ((e * BITS) >> 3)));
+        s[k] = __ldg(sw + ((e_warp + e) >> LOGB));
       }
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const int e = (k * 32 + lane) * 8;
+      for (int k = 0; k < K; ++k) {
+        const int e = k * 256 + lane * 8;
         float q[8];
         decode8<BITS>(w[k], q);
+        const float2 s2 = make_float2(s[k], s[k]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(q[i], s[k]);
+        for (int i = 0; i < 8; i += 2) {
+          const float2 v = mul2(make_float2(q[i], q[i + 1]), s2);
+          q[i] = v.x;
+          q[i + 1] = v.y;
+        }
         __stcs(reinterpret_cast<uint4*>(yw + e),
                make_uint4(pack_bf16x2(q[0], q[1]), pack_bf16x2(q[2], q[3]),
                           pack_bf16x2(q[4], q[5]), pack_bf16x2(q[6], q[7])));
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const int e = (k * 32 + lane) * 8;
+      for (int k = 0; k < K; ++k) {
+        const int e = k * 256 + lane * 8;
         for (int i = 0; i < 8; ++i) {
           const int64_t el = e_warp + e + i;
           if (el >= a.row_len) break;
           const int64_t pos = base + el;
           int q;
-          if (BITS == 8) {
+          if constexpr (BITS == 8) {
             q = (int8_t)a.codes[pos];
           } else {
             const uint8_t b = a.codes[pos >> 1];
             const int nib = (pos & 1) ? (b >> 4) : (b & 0xF);
             q = nib >= 8 ? nib - 16 : nib;
           }
-          yw[e + i] = bf16_bits(__fmul_rn((float)q, sw[el / a.block]));
+          yw[e + i] = bf16_bits(__fmul_rn((float)q, sw[el >> LOGB]));
         }
       }
+    }
+    if (++t == a.units_per_row) {
+      t = 0;
+      ++row;
     }
   }
 }
 
 template <int BITS, bool REORDER>
-cudaError_t run_quant(const QuantArgs& a, cudaStream_t st) {
-  const void* k = reinterpret_cast<const void*>(&quant_kernel<BITS, REORDER>);
-  const int wpb = a.block > kWarpElems ? a.block / kWarpElems : 1;
-  const int64_t ctas = (a.total_units + (kWarps / wpb) - 1) / (kWarps / wpb);
-  quant_kernel<BITS, REORDER><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+cudaError_t run_quant(const QuantArgs& a0, int block, cudaStream_t st) {
+  return dispatch_logb(block, [&](auto lb) -> cudaError_t {
+    constexpr int LOGB = decltype(lb)::value;
+    using G = Geo<LOGB, kQRows>;
+    QuantArgs a = a0;
+    a.units_per_row = (a.row_len + G::U - 1) / G::U;
+    a.total_units = a.total_units * a.units_per_row;  // caller passes the row count
+    const void* k = reinterpret_cast<const void*>(&quant_kernel<BITS, REORDER, LOGB>);
+    const int64_t groups = kWarps / G::WPB;
+    quant_kernel<BITS, REORDER, LOGB>
+        <<<grid_for(k, (a.total_units + groups - 1) / groups), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+  });
 }
 
 template <int BITS>
-cudaError_t run_dequant(const DequantArgs& a, cudaStream_t st) {
-  const void* k = reinterpret_cast<const void*>(&dequant_kernel<BITS>);
-  dequant_kernel<BITS><<<grid_for(k, (a.total_units + kWarps - 1) / kWarps), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
-}
-
-int64_t units_per(int64_t len, int32_t block) {
-  const int64_t U = block > kWarpElems ? block : kWarpElems;
-  return (len + U - 1) / U;
+cudaError_t run_dequant(const DequantArgs& a0, int block, cudaStream_t st) {
+  return dispatch_logb(block, [&](auto lb) -> cudaError_t {
+    constexpr int LOGB = decltype(lb)::value;
+    const void* k = reinterpret_cast<const void*>(&dequant_kernel<BITS, LOGB>);
+    dequant_kernel<BITS, LOGB>
+        <<<grid_for(k, (a0.total_units + kWarps - 1) / kWarps), kThreads, 0, st>>>(a0);
+    return cudaGetLastError();
+  });
 }
 
 }  // namespace
@@ -226,12 +274,10 @@ cudaError_t launch_qwz_quant(const uint16_t* x, int64_t nranks, int64_t shard, i
   a.x = x;
   a.codes = static_cast<uint8_t*>(codes);
   a.scales = scales;
-  a.units_per_row = units_per(shard, block);
-  a.total_units = nranks * a.units_per_row;
+  a.total_units = nranks;  // rows; scaled by units per row in run_quant
   a.row_len = shard;
   a.row_blocks = (shard + block - 1) / block;
-  a.block = block;
-  return bits == 8 ? run_quant<8, false>(a, st) : run_quant<4, false>(a, st);
+  return bits == 8 ? run_quant<8, false>(a, block, st) : run_quant<4, false>(a, block, st);
 }
 
 cudaError_t launch_qgz_reorder_quant(const uint16_t* x, int32_t N, int32_t G, int64_t bucket,
@@ -246,10 +292,8 @@ cudaError_t launch_qgz_reorder_quant(const uint16_t* x, int32_t N, int32_t G, in
   a.G = G;
   a.bucket = bucket;
   a.row_len = bucket / a.nd;
-  a.units_per_row = units_per(a.row_len, block);
-  a.total_units = (int64_t)a.nd * a.nd * a.units_per_row;
-  a.block = block;
-  return bits == 8 ? run_quant<8, true>(a, st) : run_quant<4, true>(a, st);
+  a.total_units = (int64_t)a.nd * a.nd;  // rows (rank, slice)
+  return bits == 8 ? run_quant<8, true>(a, block, st) : run_quant<4, true>(a, block, st);
 }
 
 cudaError_t launch_qwz_dequant(const void* codes, const float* scales, int64_t nranks,
@@ -259,12 +303,11 @@ cudaError_t launch_qwz_dequant(const void* codes, const float* scales, int64_t n
   a.codes = static_cast<const uint8_t*>(codes);
   a.scales = scales;
   a.y = y;
-  a.units_per_row = (shard + kWarpElems - 1) / kWarpElems;
+  a.units_per_row = (shard + 1023) / 1024;
   a.total_units = nranks * a.units_per_row;
   a.row_len = shard;
   a.row_blocks = (shard + block - 1) / block;
-  a.block = block;
-  return bits == 8 ? run_dequant<8>(a, st) : run_dequant<4>(a, st);
+  return bits == 8 ? run_dequant<8>(a, block, st) : run_dequant<4>(a, block, st);
 }
 
 }  // namespace zpp
