@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
       }
       Scale sc[NSC];
 #pragma unroll
-      for (int i = 0; i < NSC; ++i) sc[i] = make_scale(am[i * RPB], (float)QMAX);
+      for (int i = 0; i < NSC; ++i) sc[i] = make_scale<QMAX>(am[i * RPB]);
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         if (!on[k]) continue;

@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
     }
     Scale sc[G::NSC];
 #pragma unroll
-    for (int i = 0; i < G::NSC; ++i) sc[i] = make_scale(am[i * G::RPB], (float)QMAX);
+    for (int i = 0; i < G::NSC; ++i) sc[i] = make_scale<QMAX>(am[i * G::RPB]);
 
     uint8_t* cw = a.codes + (((dst_base + e_warp) * BITS) >> 3);
 #pragma unroll

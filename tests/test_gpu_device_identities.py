@@ -1,0 +1,27 @@
+"""Exhaustive GPU checks of the arithmetic identities the codec kernels use in
+place of IEEE divisions: the block scale absmax/qmax by reciprocal + one FMA
+correction equals the IEEE quotient for every non-negative float (both bit
+widths), and the refined reciprocal is within one ulp of the correctly rounded
+one for every scale the fast quantizer path accepts."""
+import os
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+pytestmark = pytest.mark.gpu
+
+
+def test_exhaustive_device_identities(tmp_path):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    exe = tmp_path / "device_checks"
+    subprocess.check_call([
+        "nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-fmad=false",
+        "-I", os.path.join(ROOT, "gradient_comm_codecs_gb300", "csrc"),
+        os.path.join(ROOT, "tests", "device_checks.cu"), "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stdout + out.stderr
+    res = {line.split()[0]: int(line.split()[1]) for line in out.stdout.splitlines()}
+    assert res == {"div_qmax7": 0, "div_qmax127": 0, "recip_1ulp": 0}, out.stdout
