@@ -141,6 +141,25 @@ def traffic_table():
     return {k: v[1] for k, v in rows.items() if cur.get(k[0]) == v[0]}
 
 
+# ---- multi-rank helpers ------------------------------------------------------------------
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest rank's time)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: int, world: int, ms_step_max: float) -> float:
+    """Whole-job throughput: bytes every replica moved per step / slowest step time."""
+    return bytes_per_rank_step * world / (ms_step_max * 1e-3) / 1e9
+
+
 # ---- clocks --------------------------------------------------------------------------
 
 class ClockSampler:
@@ -286,11 +305,7 @@ def run_gpu(args, wl, rank, world, device):
             continue
         per.setdefault(name, []).append(prev.elapsed_time(ev))
         prev = ev
-    ms_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / args.steps, device)
 
     peak, peak_kind = measured_peak()
     kernels = {}
@@ -313,7 +328,7 @@ def run_gpu(args, wl, rank, world, device):
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "traffic": traffic, "algorithmic_bytes": dk["bytes_per_launch"]}
 
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, world, ms_step)
     qgz_ms = sum(sum(per[n]) for n in per if n.startswith("qgz")) / args.steps
     qgz_eps = (g.nd * g.bucket / (qgz_ms * 1e-3)) if g else None
 
@@ -359,12 +374,8 @@ def run_e2e(args, path, wl, stream, step_bytes, world, device):
     for i in range(steps):
         h2d, d2h = path.run_from_host(w_host, g_host, p_host, stream, adam_step=3 + i)
     torch.cuda.synchronize()
-    dt = (time.perf_counter() - t0) / steps
-    if world > 1:
-        t = torch.tensor([dt], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
-    return {"value": step_bytes * world / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    dt = max_over_ranks((time.perf_counter() - t0) / steps, device)
+    return {"value": whole_job_gbs(step_bytes, world, dt * 1e3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps,
             "note": "pinned host inputs copied in and bf16 parameters copied out every step, "
                     "wall clock around the steps; value counts the same algorithmic bytes"}
