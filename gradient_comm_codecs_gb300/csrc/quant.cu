@@ -29,26 +29,167 @@ struct QuantArgs {
   int32_t nd, N, G;       // qgZ topology
 };
 
+constexpr int kQStages = 4;  // units per warp in the shared-memory prefetch ring
+constexpr size_t kQSmem = (size_t)kWarps * kQStages * kQRows * 32 * sizeof(uint4);  // 64 KiB
+
+// Quantize one warp's 1024 elements x[K][8] (lane-major rows of 256) whose
+// codes start at element `dst` of the code stream; every lane calls it.
+template <int BITS, int LOGB, class G>
+__device__ __forceinline__ void quantize_unit(float (&x)[kQRows][8], const int (&nv)[kQRows],
+                                              bool aligned, int64_t dst, int64_t scale0,
+                                              int64_t e_warp, uint8_t* __restrict__ codes,
+                                              float* __restrict__ scales, float (*red)[kWarps],
+                                              int parity, int warp, int gid, int lane) {
+  constexpr int K = kQRows;
+  constexpr int QMAX = (1 << (BITS - 1)) - 1;
+  using CW = typename CodeVec<BITS>::T;
+  float am[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const float m0 = fmaxf(fabsf(x[k][0]), fabsf(x[k][1]));
+    const float m1 = fmaxf(fabsf(x[k][2]), fabsf(x[k][3]));
+    const float m2 = fmaxf(fabsf(x[k][4]), fabsf(x[k][5]));
+    const float m3 = fmaxf(fabsf(x[k][6]), fabsf(x[k][7]));
+    am[k] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+  }
+  warp_block_absmax<G>(am);
+  if constexpr (G::WPB > 1) {
+    const float m = group_absmax<G::WPB>(am[0], red, parity, warp, gid, lane);
+#pragma unroll
+    for (int k = 0; k < K; ++k) am[k] = m;
+  }
+  Scale sc[G::NSC];
+#pragma unroll
+  for (int i = 0; i < G::NSC; ++i) sc[i] = make_scale<QMAX>(am[i * G::RPB]);
+  uint8_t* cw = codes + (((dst + e_warp) * BITS) >> 3);
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int e = k * 256 + lane * 8;
+    uint32_t c[8];
+    quantize8<QMAX>(x[k], sc[k / G::RPB], c);  // every lane: it votes
+    if (nv[k] == 0) continue;
+    const CW cv = pack8<BITS>(c);
+    uint8_t* d = cw + ((e * BITS) >> 3);
+    if (nv[k] == 8 && aligned) {
+      *reinterpret_cast<CW*>(d) = cv;
+    } else {
+      uint32_t lo, hi = 0;
+      if constexpr (BITS == 8) {
+        lo = cv.x;
+        hi = cv.y;
+      } else {
+        lo = cv;
+      }
+      const int nbytes = (nv[k] * BITS + 7) >> 3;
+      for (int i = 0; i < nbytes; ++i)
+        d[i] = (uint8_t)((i < 4 ? lo >> (8 * i) : hi >> (8 * (i - 4))) & 0xFF);
+    }
+    if (((e_warp + e) & (G::B - 1)) == 0) scales[scale0 + ((e_warp + e) >> LOGB)] = sc[k / G::RPB].s;
+  }
+}
+
+// Tiled layout: every row is a whole number of units, so unit u's input is the
+// contiguous run x[u*U + ...] (qwZ shards and qgZ slices follow one another in
+// memory).  Each warp keeps its next kQStages-1 units in flight with cp.async
+// into its own slice of shared memory: the loads never wait behind the
+// arithmetic and cost no registers.
+//
 // One row = one contiguous run quantized in blocks restarting at the row
 // start: a qwZ shard, or slice j of rank r's qgZ bucket, whose codes go to
 // slice position p = l'*N + n' (j = n'*G + l') of rank r's message.
 template <int BITS, bool REORDER, int LOGB>
-__global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
+__global__ void __launch_bounds__(kThreads) quant_tiled_kernel(const QuantArgs a) {
   using G = Geo<LOGB, kQRows>;
-  constexpr int K = kQRows;
-  constexpr int QMAX = (1 << (BITS - 1)) - 1;
-  constexpr int GPC = kWarps / G::WPB;  // warp groups per CTA
-  using CW = typename CodeVec<BITS>::T;
+  constexpr int K = kQRows, S = kQStages;
+  constexpr int GPC = kWarps / G::WPB;
   __shared__ float red[2][kWarps];
+  extern __shared__ uint4 qsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = warp / G::WPB, wsub = warp - gid * G::WPB;
+  uint4* ring = qsm + (size_t)warp * S * K * 32;  // [S][K][32]
 
   int64_t u, uend;
   unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
   if (u >= uend) return;  // the whole group shares the range
+  const uint16_t* xg = a.x + (int64_t)wsub * G::kWarpElems + lane * 8;
+  auto issue = [&](int64_t v) {
+    if (v < uend) {
+      const uint16_t* src = xg + v * G::U;
+      uint4* slot = ring + (size_t)(v & (S - 1)) * K * 32 + lane;
+#pragma unroll
+      for (int k = 0; k < K; ++k) cp_async16(slot + k * 32, src + k * 256);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < S - 1; ++i) issue(u + i);
+
+  // destination of the current unit: row = u / units_per_row, tile t
   int64_t row = u / a.units_per_row;
   int64_t t = u - row * a.units_per_row;
-  int32_t r = 0, j = 0, np = 0, lp = 0;  // qgZ: row = r*nd + j, j = np*G + lp
+  int32_t r = 0, j = 0, np = 0, lp = 0;
+  if constexpr (REORDER) {
+    r = (int32_t)(row / a.nd);
+    j = (int32_t)(row - (int64_t)r * a.nd);
+    np = j / a.G;
+    lp = j - np * a.G;
+  }
+  auto row_dst = [&]() -> int64_t {
+    if constexpr (REORDER)
+      return (int64_t)r * a.bucket + ((int64_t)lp * a.N + np) * a.row_len;
+    else
+      return row * a.row_len;
+  };
+  int64_t dst_row = row_dst();
+  const int nv[K] = {8, 8, 8, 8};
+  int parity = 0;
+
+  for (; u < uend; ++u, parity ^= 1) {
+    issue(u + S - 1);
+    cp_async_wait<S - 1>();  // this unit's copies have landed
+    float x[K][8];
+    const uint4* slot = ring + (size_t)(u & (S - 1)) * K * 32 + lane;
+#pragma unroll
+    for (int k = 0; k < K; ++k) unpack_bf16x8(slot[k * 32], x[k]);
+    const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;
+    quantize_unit<BITS, LOGB, G>(x, nv, true, dst_row, dst_row >> LOGB, e_warp, a.codes, a.scales,
+                                 red, parity, warp, gid, lane);
+    if (++t == a.units_per_row) {
+      t = 0;
+      ++row;
+      if constexpr (REORDER) {
+        ++j;
+        if (++lp == a.G) {
+          lp = 0;
+          ++np;
+        }
+        if (j == a.nd) {
+          j = np = lp = 0;
+          ++r;
+        }
+      }
+      dst_row = row_dst();
+    }
+  }
+  cp_async_wait<0>();  // no copy outlives the warp
+}
+
+// General layout (a row tail shorter than a unit, or shards whose starts are
+// not 16-byte aligned): direct loads, element loads with zero fill where needed.
+template <int BITS, bool REORDER, int LOGB>
+__global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
+  using G = Geo<LOGB, kQRows>;
+  constexpr int K = kQRows;
+  constexpr int GPC = kWarps / G::WPB;
+  __shared__ float red[2][kWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = warp / G::WPB, wsub = warp - gid * G::WPB;
+  int64_t u, uend;
+  unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
+  if (u >= uend) return;
+  int64_t row = u / a.units_per_row;
+  int64_t t = u - row * a.units_per_row;
+  int32_t r = 0, j = 0, np = 0, lp = 0;
   if constexpr (REORDER) {
     r = (int32_t)(row / a.nd);
     j = (int32_t)(row - (int64_t)r * a.nd);
@@ -56,10 +197,9 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
     lp = j - np * a.G;
   }
   int parity = 0;
-
   for (; u < uend; ++u, parity ^= 1) {
-    int64_t dst_base, scale_base;
     const int64_t src_base = row * a.row_len;
+    int64_t dst_base, scale_base;
     if constexpr (REORDER) {
       dst_base = (int64_t)r * a.bucket + ((int64_t)lp * a.N + np) * a.row_len;
       scale_base = dst_base >> LOGB;
@@ -67,79 +207,27 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
       dst_base = src_base;
       scale_base = row * a.row_blocks;
     }
-    const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;  // row-relative
+    const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;
     const int64_t valid = a.row_len - e_warp;
     const bool aligned = ((src_base | dst_base) & 7) == 0;
-    const bool full = aligned && valid >= G::kWarpElems;
     const uint16_t* xw = a.x + src_base + e_warp;
-
     float x[K][8];
     int nv[K];
-    if (full) {
-      uint4 w[K];
 #pragma unroll
-      for (int k = 0; k < K; ++k)
-        w[k] = __ldcs(reinterpret_cast<const uint4*>(xw + k * 256 + lane * 8));
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        unpack_bf16x8(w[k], x[k]);
-        nv[k] = 8;
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        const int e = k * 256 + lane * 8;
-        const int64_t rem = valid - e;
-        nv[k] = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
+    for (int k = 0; k < K; ++k) {
+      const int e = k * 256 + lane * 8;
+      const int64_t rem = valid - e;
+      nv[k] = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
+      if (nv[k] == 8 && aligned) {
+        unpack_bf16x8(__ldcs(reinterpret_cast<const uint4*>(xw + e)), x[k]);
+      } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           x[k][i] = i < nv[k] ? __uint_as_float((uint32_t)xw[e + i] << 16) : 0.0f;
       }
     }
-
-    float am[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      float m = fabsf(x[k][0]);
-#pragma unroll
-      for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(x[k][i]));
-      am[k] = m;
-    }
-    warp_block_absmax<G>(am);
-    if constexpr (G::WPB > 1) {
-      const float m = group_absmax<G::WPB>(am[0], red, parity, warp, gid, lane);
-#pragma unroll
-      for (int k = 0; k < K; ++k) am[k] = m;
-    }
-    Scale sc[G::NSC];
-#pragma unroll
-    for (int i = 0; i < G::NSC; ++i) sc[i] = make_scale<QMAX>(am[i * G::RPB]);
-
-    uint8_t* cw = a.codes + (((dst_base + e_warp) * BITS) >> 3);
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      if (nv[k] == 0) continue;
-      const int e = k * 256 + lane * 8;
-      uint32_t c[8];
-      quantize8<QMAX>(x[k], sc[k / G::RPB], c);
-      const CW w = pack8<BITS>(c);
-      uint8_t* dst = cw + ((e * BITS) >> 3);
-      if (nv[k] == 8 && aligned) {
-        *reinterpret_cast<CW*>(dst) = w;
-      } else {
-        uint32_t lo, hi = 0;
-        if constexpr (BITS == 8) {
-          lo = w.x;
-          hi = w.y;
-        } else {
-          lo = w;
-        }
-        const int nbytes = (nv[k] * BITS + 7) >> 3;
-        for (int i = 0; i < nbytes; ++i) dst[i] = (uint8_t)((i < 4 ? lo >> (8 * i) : hi >> (8 * (i - 4))) & 0xFF);
-      }
-      if (((e_warp + e) & (G::B - 1)) == 0) a.scales[scale_base + ((e_warp + e) >> LOGB)] = sc[k / G::RPB].s;
-    }
-
+    quantize_unit<BITS, LOGB, G>(x, nv, aligned, dst_base, scale_base, e_warp, a.codes, a.scales,
+                                 red, parity, warp, gid, lane);
     if (++t == a.units_per_row) {
       t = 0;
       ++row;
@@ -247,10 +335,18 @@ cudaError_t run_quant(const QuantArgs& a0, int block, cudaStream_t st) {
     QuantArgs a = a0;
     a.units_per_row = (a.row_len + G::U - 1) / G::U;
     a.total_units = a.total_units * a.units_per_row;  // caller passes the row count
-    const void* k = reinterpret_cast<const void*>(&quant_kernel<BITS, REORDER, LOGB>);
     const int64_t groups = kWarps / G::WPB;
-    quant_kernel<BITS, REORDER, LOGB>
-        <<<grid_for(k, (a.total_units + groups - 1) / groups), kThreads, 0, st>>>(a);
+    const int64_t ctas = (a.total_units + groups - 1) / groups;
+    if (a.row_len % G::U == 0) {  // tiled: every unit full, 16-byte aligned
+      const void* k = reinterpret_cast<const void*>(&quant_tiled_kernel<BITS, REORDER, LOGB>);
+      static const cudaError_t attr =
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmem);
+      if (attr != cudaSuccess) return attr;
+      quant_tiled_kernel<BITS, REORDER, LOGB><<<grid_for(k, ctas, kQSmem), kThreads, kQSmem, st>>>(a);
+    } else {
+      const void* k = reinterpret_cast<const void*>(&quant_kernel<BITS, REORDER, LOGB>);
+      quant_kernel<BITS, REORDER, LOGB><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+    }
     return cudaGetLastError();
   });
 }
