@@ -208,6 +208,167 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
   }
 }
 
+// Tiled layout (every destination row a whole number of units, true whenever
+// the slice length is a multiple of 1024): per-row source base pointers, no
+// per-element 64-bit address arithmetic and no tail predication.  Sources are
+// read two at a time, the next pair's loads in flight while the current pair
+// is summed.
+template <int BITS, int MODE, int LOGB>
+__global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a) {
+  using C = HopCfg<BITS, MODE, LOGB>;
+  using G = typename C::G;
+  constexpr int K = C::K, WPB = C::WPB, NSC = G::NSC, RPB = G::RPB;
+  // requant: two sources per chunk (registers); final hops: the state loads
+  // need deeper prefetch, four int4 sources per chunk
+  constexpr int SCH = (MODE == kRequant || BITS == 8) ? 2 : 4;
+  constexpr int QMAX = (1 << (BITS - 1)) - 1;
+  constexpr int GPC = kWarps / WPB;
+  constexpr int ROWB = 256 * BITS / 8;  // code bytes of one 256-element row
+  using CW = typename CodeVec<BITS>::T;
+  using CH = Chunk<BITS, K, NSC, SCH>;
+  __shared__ float red[2][kWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = warp / WPB, wsub = warp - gid * WPB;
+
+  int64_t u, uend;
+  unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
+  if (u >= uend) return;
+  int64_t d = u / a.units_per_row;
+  int64_t t = u - d * a.units_per_row;
+  int32_t dn = (int32_t)(d / a.G), dl = (int32_t)(d - (int64_t)dn * a.G);
+  // source s of destination d starts at element (src0 + s*sstride)*in_rank_elems + in_off
+  const int64_t sstep = (a.hop == 1 ? 1 : (int64_t)a.G) * a.in_rank_elems;
+  const int64_t cstep = (sstep * BITS) >> 3;   // bytes between consecutive sources
+  const int64_t fstep = sstep >> LOGB;         // scales between consecutive sources
+  const uint8_t* crow;
+  const float* srow;
+  auto row_bases = [&]() {
+    const int64_t src0 = a.hop == 1 ? (int64_t)dn * a.G : dl;
+    const int64_t e0 = src0 * a.in_rank_elems + (a.hop == 1 ? (int64_t)dl : (int64_t)dn) * a.R;
+    crow = a.codes_in + ((e0 * BITS) >> 3) + lane * (8 * BITS / 8);
+    srow = a.scales_in + (e0 >> LOGB);
+  };
+  row_bases();
+  // scale of row k's block for this lane, relative to the unit's first scale
+  int soff[NSC];
+#pragma unroll
+  for (int i = 0; i < NSC; ++i) soff[i] = (i * RPB * 256 + lane * 8) >> LOGB;
+  int parity = 0;
+
+  for (; u < uend; ++u, parity ^= 1) {
+    const int64_t e_warp = t * C::U + (int64_t)wsub * G::kWarpElems;
+    const int64_t obase = d * a.R + e_warp;
+    const uint8_t* cu = crow + ((e_warp * BITS) >> 3);
+    const float* su = srow + (e_warp >> LOGB);
+
+    AdamVec st[MODE == kFinalAdam ? K : 1];
+    if constexpr (MODE == kFinalAdam) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) st[k] = adam_load8(obase + k * 256 + lane * 8, a.master, a.m, a.v);
+    }
+    auto load = [&](CH& ch, int s0) {
+#pragma unroll
+      for (int j = 0; j < SCH; ++j) {
+        const int s = s0 + j;
+        if (s < a.S) {
+          const uint8_t* cs = cu + (int64_t)s * cstep;
+          const float* ss = su + (int64_t)s * fstep;
+#pragma unroll
+          for (int k = 0; k < K; ++k) ch.c[j][k] = __ldcs(reinterpret_cast<const CW*>(cs + k * ROWB));
+#pragma unroll
+          for (int i = 0; i < NSC; ++i) ch.s[j][i] = __ldg(ss + soff[i]);
+        }
+      }
+    };
+    float acc[K][8];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[k][i] = 0.0f;
+    auto sum = [&](const CH& ch, int s0) {
+#pragma unroll
+      for (int j = 0; j < SCH; ++j) {
+        if (s0 + j >= a.S) break;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          float q[8];
+          decode8<BITS>(ch.c[j][k], q);
+          accumulate8(acc[k], q, ch.s[j][k / RPB]);
+        }
+      }
+    };
+    CH ca, cb;
+    load(ca, 0);
+    for (int c = 0; c < a.S; c += 2 * SCH) {
+      if (c + SCH < a.S) load(cb, c + SCH);
+      sum(ca, c);
+      if (c + SCH >= a.S) break;
+      if (c + 2 * SCH < a.S) load(ca, c + 2 * SCH);
+      sum(cb, c + SCH);
+    }
+
+    if constexpr (MODE == kRequant) {
+      float am[K];
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const float m0 = fmaxf(fabsf(acc[k][0]), fabsf(acc[k][1]));
+        const float m1 = fmaxf(fabsf(acc[k][2]), fabsf(acc[k][3]));
+        const float m2 = fmaxf(fabsf(acc[k][4]), fabsf(acc[k][5]));
+        const float m3 = fmaxf(fabsf(acc[k][6]), fabsf(acc[k][7]));
+        am[k] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+      }
+      warp_block_absmax<G>(am);
+      if constexpr (WPB > 1) {
+        const float m = group_absmax<WPB>(am[0], red, parity, warp, gid, lane);
+#pragma unroll
+        for (int k = 0; k < K; ++k) am[k] = m;
+      }
+      Scale sc[NSC];
+#pragma unroll
+      for (int i = 0; i < NSC; ++i) sc[i] = make_scale<QMAX>(am[i * RPB]);
+      uint8_t* co = a.codes_out + ((obase * BITS) >> 3) + lane * (8 * BITS / 8);
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        uint32_t c[8];
+        quantize8<QMAX>(acc[k], sc[k / RPB], c);
+        *reinterpret_cast<CW*>(co + k * ROWB) = pack8<BITS>(c);
+        const int e = k * 256 + lane * 8;
+        if (((e_warp + e) & (G::B - 1)) == 0) a.scales_out[(obase + e) >> LOGB] = sc[k / RPB].s;
+      }
+    } else {
+      const float2 inv = make_float2(a.inv_nd, a.inv_nd);
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const int64_t idx = obase + k * 256 + lane * 8;
+        float g[8];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const float2 v = mul2(make_float2(acc[k][i], acc[k][i + 1]), inv);
+          g[i] = v.x;
+          g[i + 1] = v.y;
+        }
+        if (a.grad_out) {
+          float4* go = reinterpret_cast<float4*>(a.grad_out + idx);
+          __stcs(go, make_float4(g[0], g[1], g[2], g[3]));
+          __stcs(go + 1, make_float4(g[4], g[5], g[6], g[7]));
+        }
+        if constexpr (MODE == kFinalAdam)
+          adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac);
+      }
+    }
+
+    if (++t == a.units_per_row) {
+      t = 0;
+      ++d;
+      if (++dl == a.G) {
+        dl = 0;
+        ++dn;
+      }
+      row_bases();
+    }
+  }
+}
+
 template <int BITS, int MODE>
 cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
   return dispatch_logb(block, [&](auto lb) -> cudaError_t {
@@ -216,10 +377,15 @@ cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
     HopArgs a = a0;
     a.units_per_row = (a.R + C::U - 1) / C::U;
     a.total_units = (int64_t)a.N * a.G * a.units_per_row;
-    const void* k = reinterpret_cast<const void*>(&hop_kernel<BITS, MODE, LOGB>);
     const int64_t groups = kWarps / C::WPB;
-    hop_kernel<BITS, MODE, LOGB>
-        <<<grid_for(k, (a.total_units + groups - 1) / groups), kThreads, 0, st>>>(a);
+    const int64_t ctas = (a.total_units + groups - 1) / groups;
+    if (a.R % C::U == 0) {
+      const void* k = reinterpret_cast<const void*>(&hop_tiled_kernel<BITS, MODE, LOGB>);
+      hop_tiled_kernel<BITS, MODE, LOGB><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+    } else {
+      const void* k = reinterpret_cast<const void*>(&hop_kernel<BITS, MODE, LOGB>);
+      hop_kernel<BITS, MODE, LOGB><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+    }
     return cudaGetLastError();
   });
 }
