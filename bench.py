@@ -496,6 +496,104 @@ def run_reference(args, wl):
     }
 
 
+# ---- the sweep (small-message efficiency) -----------------------------------------------------
+
+def run_sweep(args):
+    """Every sweep point: qgZ chain (reorder+quant, hop 1, hop 2 / final, no
+    Adam) and qwZ quant+dequant on N_d shards of the same size, timed with
+    CUDA events (plain launches) and, for the qgZ chain, as a CUDA-graph
+    replay.  Timing inputs are filled in place by torch's normal_ (bf16,
+    N(0, 1e-3) gradients, N(0, 0.02) weights); parity of sweep points is
+    covered by the tests.  Points whose buffers do not fit in free memory are
+    skipped and reported as such."""
+    import torch
+    import gradient_comm_codecs_gb300 as Z
+    from gradient_comm_codecs_gb300 import _build
+    from synth import workloads as W
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    out = []
+    for i, wl in W.sweep_points():
+        q, g = wl.qwz, wl.qgz
+        if g.bucket * 2 > args.sweep_max_mib << 20:
+            continue
+        rec = {"index": i, "block": g.block, "bits": g.bits, "N_d": g.nd,
+               "topology": f"{g.nodes}x{g.gpus_per_node}", "mib_per_rank": g.bucket * 2 >> 20}
+        nd, b = g.nd, g.bucket
+        c = g.bits / 8 + 4 / g.block
+        need = nd * b * (2 + c) + nd * g.nodes * g.slice_elems * c + 4 * b
+        free, _ = torch.cuda.mem_get_info(dev)
+        if need > 0.85 * free:
+            rec["skipped"] = f"needs {need / 2**30:.0f} GiB"
+            out.append(rec)
+            print(json.dumps(rec), flush=True)
+            continue
+        torch.manual_seed(i)
+        path = Z.CodecPath(None, Z.QgzSpec(g.nodes, g.gpus_per_node, b, g.block, g.bits), None,
+                           device=dev, keep_grad=True)
+        path.grads.normal_(0.0, 1e-3)  # in place: no temporary
+        qgz_bytes = sum(x for n, x in launch_bytes(wl) if n.startswith("qgz"))
+        st = torch.cuda.current_stream(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        path.run_qgz(st)
+        torch.cuda.synchronize()
+        e0.record(st)
+        path.run_qgz(st)
+        e1.record(st)
+        torch.cuda.synchronize()
+        once = e0.elapsed_time(e1)
+        iters = max(3, min(200, int(200.0 / max(once, 1e-3))))
+        e0.record(st)
+        for _ in range(iters):
+            path.run_qgz(st)
+        e1.record(st)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        rec.update(qgz_ms=ms, qgz_gbs=qgz_bytes / (ms * 1e-3) / 1e9,
+                   qgz_elems_per_s=nd * b / (ms * 1e-3))
+        # CUDA-graph replay of the same chain (launch overhead removed)
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(st)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            path.run_qgz(gs)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=gs):
+                path.run_qgz(gs)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(iters):
+            graph.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        gms = e0.elapsed_time(e1) / iters
+        rec.update(qgz_graph_ms=gms, qgz_graph_gbs=qgz_bytes / (gms * 1e-3) / 1e9)
+        del graph, path
+        torch.cuda.empty_cache()
+        # qwZ on N_d shards of the same size
+        if nd * b * (4 + c) < 0.85 * torch.cuda.mem_get_info(dev)[0]:
+            qp = Z.CodecPath(Z.QwzSpec(q.nranks, q.shard, q.block, q.bits), None, None, device=dev)
+            qp.w.normal_(0.0, 0.02)
+            qwz_bytes = sum(x for n, x in launch_bytes(wl) if n.startswith("qwz"))
+            qp.run_qwz(st)
+            torch.cuda.synchronize()
+            e0.record(st)
+            for _ in range(iters):
+                qp.run_qwz(st)
+            e1.record(st)
+            torch.cuda.synchronize()
+            qms = e0.elapsed_time(e1) / iters
+            rec.update(qwz_ms=qms, qwz_gbs=qwz_bytes / (qms * 1e-3) / 1e9)
+            del qp
+            torch.cuda.empty_cache()
+        out.append(rec)
+        print(json.dumps(rec), flush=True)
+    return out
+
+
 # ---- main ------------------------------------------------------------------------------------
 
 def main():
@@ -507,6 +605,9 @@ def main():
     ap.add_argument("--config", default="llama", choices=["tiny", "llama", "two_hop", "7b"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the 144-point block/bits/topology/message-size sweep instead")
+    ap.add_argument("--sweep-max-mib", type=int, default=1024)
     ap.add_argument("--scale", type=int, default=1,
                     help="divide the workload's shard and bucket by this (small profiling cases)")
     args = ap.parse_args()
@@ -518,6 +619,9 @@ def main():
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, wl)), flush=True)
