@@ -41,14 +41,15 @@ NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 KERNEL_OF = {  # launch name -> CUDA kernel (for the roofline and the ncu summaries)
-    "qwz_quant": "quant_kernel<BITS, false>",
-    "qwz_dequant": "dequant_kernel<BITS>",
-    "qgz_reorder_quant": "quant_kernel<BITS, true>",
-    "qgz_hop1": "hop_kernel<BITS, 0>",
-    "qgz_final_hop": "hop_kernel<BITS, 1>",
+    "qwz_quant": "quant_tiled_kernel<BITS, false, LOGB>",
+    "qwz_dequant": "dequant_kernel<BITS, LOGB>",
+    "qgz_reorder_quant": "quant_tiled_kernel<BITS, true, LOGB>",
+    "qgz_hop1": "hop_tiled_kernel<BITS, kRequant, LOGB>",
+    "qgz_final_hop": "hop_tiled_kernel<BITS, kFinalAdam, LOGB>",
+    "qgz_final_hop_qwz": "hop_tiled_kernel<BITS, kFinalAdamQwz, LOGB>",
 }
 KERNEL_SRC = {"qwz_quant": "quant.cu", "qwz_dequant": "quant.cu", "qgz_reorder_quant": "quant.cu",
-              "qgz_hop1": "hop.cu", "qgz_final_hop": "hop.cu"}
+              "qgz_hop1": "hop.cu", "qgz_final_hop": "hop.cu", "qgz_final_hop_qwz": "hop.cu"}
 
 
 # ---- workload -> algorithmic bytes ------------------------------------------------
@@ -61,11 +62,16 @@ def msg_bytes(n, block, bits):
     return codes_bytes(n, bits) + 4 * (-(-n // block))
 
 
-def launch_bytes(wl):
-    """[(launch name, algorithmic bytes)] of one pass, in launch order."""
+def launch_bytes(wl, fuse_qwz=False):
+    """[(launch name, algorithmic bytes)] of one pass, in launch order.  With
+    fuse_qwz the weights' qwZ message is written by the final hop's Adam pass
+    (the next step's message), so the pass has no separate quantize launch."""
     out = []
     q, g = wl.qwz, wl.qgz
-    if q is not None:
+    if q is not None and fuse_qwz:
+        m = q.nranks * msg_bytes(q.shard, q.block, q.bits)
+        out.append(("qwz_dequant", m + 2 * q.nranks * q.shard))
+    elif q is not None:
         shards = [q.shard] * q.calls
         if q.tail_shard:
             shards[-1] = q.tail_shard
@@ -78,18 +84,24 @@ def launch_bytes(wl):
         m1 = nd * msg_bytes(b, g.block, g.bits)
         out.append(("qgz_reorder_quant", 2 * nd * b + m1))
         final_extra = (26 * b) if wl.fused_adam else 4 * b
+        name = "qgz_final_hop"
+        if fuse_qwz:
+            final_extra += nd * msg_bytes(g.slice_elems, g.block, 8)
+            name = "qgz_final_hop_qwz"
         if g.nodes == 1:
-            out.append(("qgz_final_hop", m1 + final_extra))
+            out.append((name, m1 + final_extra))
         else:
             m2 = nd * msg_bytes(g.nodes * g.slice_elems, g.block, g.bits)
             out.append(("qgz_hop1", m1 + m2))
-            out.append(("qgz_final_hop", m2 + final_extra))
+            out.append((name, m2 + final_extra))
     return out
 
 
-def workload_config(wl, name):
+def workload_config(wl, name, fuse_qwz=False):
     q, g = wl.qwz, wl.qgz
     cfg = {"workload": wl.name, "name": name}
+    if fuse_qwz:
+        cfg["qwz_fused"] = "the weights' int8 qwZ message is written by the final hop's Adam pass"
     if q is not None:
         cfg.update(qwz_phi=q.phi, qwz=f"int{q.bits} B={q.block}", qwz_nranks=q.nranks,
                    qwz_calls=q.calls)
@@ -97,7 +109,7 @@ def workload_config(wl, name):
         cfg.update(N_d=g.nd, topology=f"{g.nodes}x{g.gpus_per_node}", bucket_per_rank=g.bucket,
                    qgz=f"int{g.bits} B={g.block}", adam="fused on the final hop" if wl.fused_adam
                    else "none")
-    per_step = sum(b for _, b in launch_bytes(wl))
+    per_step = sum(b for _, b in launch_bytes(wl, fuse_qwz))
     if per_step > 4 * L2_BYTES:
         cfg["l2"] = (f"inputs larger than L2: {per_step / 1e9:.2f} GB moved per step vs "
                      f"{L2_BYTES / 2**20:.0f} MiB L2; no flush")
@@ -250,10 +262,12 @@ def run_gpu(args, wl, rank, world, device):
     gs = Z.QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits) if g else None
     a = wl.adam
     adam = Z.AdamSpec(a.lr, a.beta1, a.beta2, a.eps, a.step) if (g and wl.fused_adam) else None
-    path = Z.CodecPath(qs, gs, adam, device=device, keep_grad=False)
+    path = Z.CodecPath(qs, gs, adam, device=device, keep_grad=False, fuse_qwz=args.fuse_qwz)
     fill_inputs(path, wl)
     stream = torch.cuda.current_stream(device)
-    lb = launch_bytes(wl)
+    if args.fuse_qwz:
+        path.prime_fused_qwz(stream)
+    lb = launch_bytes(wl, args.fuse_qwz)
     step_bytes = sum(b for _, b in lb)
 
     def one_step(i, events=None):
@@ -320,7 +334,7 @@ def run_gpu(args, wl, rank, world, device):
                          "frac_of_peak": nb / (avg * 1e-3) / 1e9 / peak,
                          "share": sum(ts) / total_ms}
     dom = max(kernels, key=lambda k: kernels[k]["share"])
-    traffic = traffic_table().get((dom, args.config))
+    traffic = traffic_table().get((dom, args.config + ("+fuse_qwz" if args.fuse_qwz else "")))
     dk = kernels[dom]
     roofline = {"bound": "hbm", "kernel": dk["kernel"], "launch": dom,
                 "achieved": dk["gbs"], "peak": peak, "unit": "GB/s",
@@ -343,7 +357,7 @@ def run_gpu(args, wl, rank, world, device):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic: seeded counter-based generator (lowbias32 hash -> "
         "2^20-entry quantile table), weights N(0,0.02), grads per the workload",
-        "config": workload_config(wl, args.config),
+        "config": workload_config(wl, args.config, args.fuse_qwz),
         "pct_hbm_peak_measured": 100.0 * value / world / peak,
         "pct_hbm_peak_nominal": 100.0 * value / world / NOMINAL_HBM_GBS,
         "qgz_bucket_elems_per_s": qgz_eps * world if qgz_eps else None,
@@ -359,7 +373,8 @@ def run_gpu(args, wl, rank, world, device):
 def run_e2e(args, path, wl, stream, step_bytes, world, device):
     import torch
     steps = max(3, min(args.steps, 30))
-    w_host = path.w.cpu().pin_memory() if path.qwz is not None else None
+    # fused mode: the step's weight message comes from the previous step on the device
+    w_host = path.w.cpu().pin_memory() if (path.qwz is not None and not path.fuse_qwz) else None
     g_host = path.grads.cpu().pin_memory() if path.qgz is not None else None
     p_host = None
     if path.qgz is not None and path.adam is not None:
@@ -604,6 +619,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama", choices=["tiny", "llama", "two_hop", "7b"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fuse-qwz", action="store_true",
+                    help="produce the weights' qwZ message inside the final hop's Adam pass")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="run the 144-point block/bits/topology/message-size sweep instead")

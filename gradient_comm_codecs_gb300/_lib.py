@@ -22,7 +22,7 @@ ZPP_OK, ZPP_ERR_INVALID_ARG, ZPP_ERR_MISALIGNED, ZPP_ERR_UNSUPPORTED, ZPP_ERR_CU
 # every symbol include/zpp.h declares
 EXPORTS = (
     "zpp_qwz_quant", "zpp_qwz_dequant", "zpp_qgz_reorder_quant", "zpp_qgz_hop_reduce",
-    "zpp_shard_adam_step", "zpp_codes_bytes", "zpp_num_blocks", "zpp_qgz_slice_perm",
+    "zpp_qgz_final_hop_adam_qwz", "zpp_shard_adam_step", "zpp_codes_bytes", "zpp_num_blocks", "zpp_qgz_slice_perm",
     "zpp_status_string", "zpp_last_cuda_error", "zpp_abi_version",
 )
 
@@ -69,6 +69,8 @@ def _lib():
         "zpp_qwz_dequant": (I32, [P, P, I64, I64, I32, I32, P, P]),
         "zpp_qgz_reorder_quant": (I32, [P, I32, I32, I64, I32, I32, P, P, P]),
         "zpp_qgz_hop_reduce": (I32, [I32, P, P, I32, I32, I64, I32, I32, P, P, P, HP, ST, P]),
+        "zpp_qgz_final_hop_adam_qwz": (I32, [I32, P, P, I32, I32, I64, I32, I32, P, HP, ST, I32, P,
+                                              P, P]),
         "zpp_shard_adam_step": (I32, [P, I64, HP, ST, P]),
         "zpp_codes_bytes": (I64, [I64, I32]),
         "zpp_num_blocks": (I64, [I64, I32]),
@@ -173,6 +175,17 @@ def zpp_qgz_hop_reduce(hop, codes_in, scales_in, nodes, gpus_per_node, bucket_el
                                      _dev(scales_out, _F32, "scales_out"),
                                      _dev(grad_out, _F32, "grad_out"), hp, st,
                                      _stream(stream, codes_in)), "zpp_qgz_hop_reduce")
+
+
+def zpp_qgz_final_hop_adam_qwz(hop, codes_in, scales_in, nodes, gpus_per_node, bucket_elems,
+                               block, bits, grad_out, adam, state, qwz_bits, qwz_codes,
+                               qwz_scales, stream=None):
+    hp, st, _keep1, _keep2 = _adam_args(adam, state)
+    _check(_lib().zpp_qgz_final_hop_adam_qwz(
+        hop, _dev(codes_in, _BYTES, "codes_in"), _dev(scales_in, _F32, "scales_in"), nodes,
+        gpus_per_node, bucket_elems, block, bits, _dev(grad_out, _F32, "grad_out"), hp, st,
+        qwz_bits, _dev(qwz_codes, _BYTES, "qwz_codes"), _dev(qwz_scales, _F32, "qwz_scales"),
+        _stream(stream, codes_in)), "zpp_qgz_final_hop_adam_qwz")
 
 
 def zpp_shard_adam_step(grad, n, adam, state, stream=None):

@@ -38,18 +38,24 @@ struct HopArgs {
   float* m;
   float* v;
   uint16_t* param;
+  uint8_t* qwz_codes;      // final hop + Adam + qwZ: next step's weight message
+  float* qwz_scales;
 };
 
-enum { kRequant = 0, kFinal = 1, kFinalAdam = 2 };
+// kFinalAdamQwz: the final hop, the Adam step, and the int8 block
+// quantization of the new bf16 parameters (the next forward all-gather's qwZ
+// message, blocks restarting at every rank's owned shard) in one pass.
+enum { kRequant = 0, kFinal = 1, kFinalAdam = 2, kFinalAdamQwz = 3 };
 
 template <int MODE>
-constexpr int hop_rows() { return MODE == kFinalAdam ? 2 : 4; }
+constexpr int hop_rows() { return MODE >= kFinalAdam ? 2 : 4; }
 
 template <int BITS, int MODE, int LOGB>
 struct HopCfg {
   static constexpr int K = hop_rows<MODE>();
   using G = Geo<LOGB, K>;
-  static constexpr int WPB = MODE == kRequant ? G::WPB : 1;   // final hops need no block absmax
+  // the requantizing modes need whole blocks per warp group; plain final hops do not
+  static constexpr int WPB = (MODE == kRequant || MODE == kFinalAdamQwz) ? G::WPB : 1;
   static constexpr int U = WPB * G::kWarpElems;
   static constexpr int SCH = BITS == 4 ? 4 : 2;                // sources per load chunk
 };
@@ -261,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
     const uint8_t* cu = crow + ((e_warp * BITS) >> 3);
     const float* su = srow + (e_warp >> LOGB);
 
-    AdamVec st[MODE == kFinalAdam ? K : 1];
-    if constexpr (MODE == kFinalAdam) {
+    AdamVec st[MODE >= kFinalAdam ? K : 1];
+    if constexpr (MODE >= kFinalAdam) {
 #pragma unroll
       for (int k = 0; k < K; ++k) st[k] = adam_load8(obase + k * 256 + lane * 8, a.master, a.m, a.v);
     }
@@ -337,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
       }
     } else {
       const float2 inv = make_float2(a.inv_nd, a.inv_nd);
+      float pq[MODE == kFinalAdamQwz ? K : 1][8];
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int64_t idx = obase + k * 256 + lane * 8;
@@ -354,6 +361,36 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
         }
         if constexpr (MODE == kFinalAdam)
           adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac);
+        if constexpr (MODE == kFinalAdamQwz)
+          adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac, pq[k]);
+      }
+      if constexpr (MODE == kFinalAdamQwz) {
+        float am[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const float m0 = fmaxf(fabsf(pq[k][0]), fabsf(pq[k][1]));
+          const float m1 = fmaxf(fabsf(pq[k][2]), fabsf(pq[k][3]));
+          const float m2 = fmaxf(fabsf(pq[k][4]), fabsf(pq[k][5]));
+          const float m3 = fmaxf(fabsf(pq[k][6]), fabsf(pq[k][7]));
+          am[k] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+        }
+        warp_block_absmax<G>(am);
+        if constexpr (WPB > 1) {
+          const float m = group_absmax<WPB>(am[0], red, parity, warp, gid, lane);
+#pragma unroll
+          for (int k = 0; k < K; ++k) am[k] = m;
+        }
+        Scale sc[NSC];
+#pragma unroll
+        for (int i = 0; i < NSC; ++i) sc[i] = make_scale<127>(am[i * RPB]);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          uint32_t c[8];
+          quantize8<127>(pq[k], sc[k / RPB], c);
+          const int e = k * 256 + lane * 8;
+          *reinterpret_cast<uint2*>(a.qwz_codes + obase + e) = pack_i8x8(c);
+          if (((e_warp + e) & (G::B - 1)) == 0) a.qwz_scales[(obase + e) >> LOGB] = sc[k / RPB].s;
+        }
       }
     }
 
@@ -382,6 +419,8 @@ cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
     if (a.R % C::U == 0) {
       const void* k = reinterpret_cast<const void*>(&hop_tiled_kernel<BITS, MODE, LOGB>);
       hop_tiled_kernel<BITS, MODE, LOGB><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+    } else if constexpr (MODE == kFinalAdamQwz) {
+      return cudaErrorNotSupported;
     } else {
       const void* k = reinterpret_cast<const void*>(&hop_kernel<BITS, MODE, LOGB>);
       hop_kernel<BITS, MODE, LOGB><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
@@ -415,8 +454,12 @@ cudaError_t launch_hop_reduce(const HopLaunch& h, cudaStream_t st) {
   a.m = h.m;
   a.v = h.v;
   a.param = h.param;
+  a.qwz_codes = static_cast<uint8_t*>(h.qwz_codes);
+  a.qwz_scales = h.qwz_scales;
   const int b = h.block;
   if (!final_hop) return h.bits == 8 ? run_hop<8, kRequant>(a, b, st) : run_hop<4, kRequant>(a, b, st);
+  if (h.adam && h.qwz_codes)
+    return h.bits == 8 ? run_hop<8, kFinalAdamQwz>(a, b, st) : run_hop<4, kFinalAdamQwz>(a, b, st);
   if (h.adam) return h.bits == 8 ? run_hop<8, kFinalAdam>(a, b, st) : run_hop<4, kFinalAdam>(a, b, st);
   return h.bits == 8 ? run_hop<8, kFinal>(a, b, st) : run_hop<4, kFinal>(a, b, st);
 }

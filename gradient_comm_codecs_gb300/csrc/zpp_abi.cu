@@ -233,6 +233,52 @@ zpp_status zpp_qgz_hop_reduce(int32_t hop, const void* codes_in, const float* sc
   return cuda_status(launch_hop_reduce(h, static_cast<cudaStream_t>(stream)));
 }
 
+zpp_status zpp_qgz_final_hop_adam_qwz(int32_t hop, const void* codes_in, const float* scales_in,
+                                      int32_t nodes, int32_t gpus_per_node,
+                                      int64_t bucket_elems, int32_t block, int32_t bits,
+                                      float* grad_out, const zpp_adam_hparams* adam,
+                                      const zpp_adam_state* state, int32_t qwz_bits,
+                                      void* qwz_codes, float* qwz_scales, void* stream) {
+  zpp_status s = check_topology(nodes, gpus_per_node, bucket_elems, block, bits);
+  if (s != ZPP_OK) return s;
+  if (hop != 1 && hop != 2) return ZPP_ERR_INVALID_ARG;
+  if ((hop == 2) != (nodes > 1)) return ZPP_ERR_INVALID_ARG;  // must be the final hop
+  if (!adam || !state) return ZPP_ERR_INVALID_ARG;
+  if (qwz_bits != 8) return qwz_bits == 4 ? ZPP_ERR_UNSUPPORTED : ZPP_ERR_INVALID_ARG;
+  HopLaunch h{};
+  s = adam_consts(adam, &h.ac);
+  if (s != ZPP_OK) return s;
+  s = check_state(state);
+  if (s != ZPP_OK) return s;
+  const int64_t nd = (int64_t)nodes * gpus_per_node;
+  const int64_t L = bucket_elems / nd;
+  const int64_t unit = block > 512 ? block : 512;
+  if (L % unit != 0) return ZPP_ERR_UNSUPPORTED;
+  if (bucket_elems == 0) return ZPP_OK;
+  if (!codes_in || !scales_in || !qwz_codes || !qwz_scales) return ZPP_ERR_INVALID_ARG;
+  if (!aligned16(codes_in) || !aligned16(scales_in) || !aligned16(qwz_codes) ||
+      !aligned16(qwz_scales) || (grad_out && !aligned16(grad_out)))
+    return ZPP_ERR_MISALIGNED;
+  h.hop = hop;
+  h.codes_in = codes_in;
+  h.scales_in = scales_in;
+  h.N = nodes;
+  h.G = gpus_per_node;
+  h.bucket = bucket_elems;
+  h.block = block;
+  h.bits = bits;
+  h.grad_out = grad_out;
+  h.inv_nd = 1.0f / (float)nd;
+  h.adam = true;
+  h.master = state->master;
+  h.m = state->m;
+  h.v = state->v;
+  h.param = state->param_bf16;
+  h.qwz_codes = qwz_codes;
+  h.qwz_scales = qwz_scales;
+  return cuda_status(launch_hop_reduce(h, static_cast<cudaStream_t>(stream)));
+}
+
 zpp_status zpp_shard_adam_step(const float* grad, int64_t n, const zpp_adam_hparams* hp,
                                const zpp_adam_state* st, void* stream) {
   if (n < 0 || n > kMaxElems) return ZPP_ERR_INVALID_ARG;

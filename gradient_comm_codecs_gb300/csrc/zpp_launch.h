@@ -45,6 +45,8 @@ struct HopLaunch {
   float* m;
   float* v;
   uint16_t* param;
+  void* qwz_codes;        // fused int8 qwZ of the new parameters (final hop + Adam), optional
+  float* qwz_scales;
 };
 cudaError_t launch_hop_reduce(const HopLaunch& h, cudaStream_t st);
 

@@ -84,8 +84,20 @@ class CodecPath:
     """
 
     def __init__(self, qwz: QwzSpec | None, qgz: QgzSpec | None, adam: AdamSpec | None,
-                 device="cuda", keep_grad: bool = False, write_param: bool = True):
+                 device="cuda", keep_grad: bool = False, write_param: bool = True,
+                 fuse_qwz: bool = False):
+        """fuse_qwz: the weights' qwZ message is produced by the final hop's
+        Adam pass from the new parameters (zpp_qgz_final_hop_adam_qwz) instead
+        of a separate quantize call; needs the qwZ shards to be the ranks'
+        owned qgZ slices (nranks = N_d, shard = L, same block, int8)."""
         self.qwz, self.qgz, self.adam = qwz, qgz, adam
+        self.fuse_qwz = fuse_qwz
+        if fuse_qwz:
+            ok = (qwz is not None and qgz is not None and adam is not None and qwz.bits == 8
+                  and qwz.chunks == 1 and qwz.nranks == qgz.nd and qwz.shard == qgz.L
+                  and qwz.block == qgz.block)
+            if not ok:
+                raise ValueError("fuse_qwz needs qwZ shards equal to the owned qgZ slices")
         self.device = torch.device(device)
         dev = self.device
         self.launches_per_run = 0
@@ -98,7 +110,7 @@ class CodecPath:
             self.w_scales = [_empty(qwz.nranks * Z.zpp_num_blocks(s, qwz.block), torch.float32, dev)
                              for s in sorted(set(shards))]
             self.w_full = _empty(qwz.phi, torch.bfloat16, dev)
-            self.launches_per_run += 2 * len(shards)
+            self.launches_per_run += (1 if fuse_qwz else 2) * len(shards)
         if qgz is not None:
             nd, b = qgz.nd, qgz.bucket
             self.grads = _empty(nd * b, torch.bfloat16, dev)
@@ -120,8 +132,20 @@ class CodecPath:
     # ---- the pass ---------------------------------------------------------------
     # `mark(name)`, when given, is called after each launch (the bench records a
     # CUDA event there to time every kernel of the pass).
+    def prime_fused_qwz(self, stream=None):
+        """Fused mode: the first step's weight message, from the initial weights."""
+        q = self.qwz
+        Z.zpp_qwz_quant(self.w, q.nranks, q.shard, q.block, q.bits, self.w_codes[0],
+                        self.w_scales[0], stream)
+
     def run_qwz(self, stream=None, mark=None):
         q = self.qwz
+        if self.fuse_qwz:  # the message was written by the previous step's Adam pass
+            Z.zpp_qwz_dequant(self.w_codes[0], self.w_scales[0], q.nranks, q.shard, q.block,
+                              q.bits, self.w_full, stream)
+            if mark:
+                mark("qwz_dequant")
+            return
         off = 0
         for s in q.call_shards():
             n = q.nranks * s
@@ -150,7 +174,21 @@ class CodecPath:
                 hp[4] = adam_step
             adam = tuple(hp)
             state = (self.master, self.m, self.v, self.param)
-        if g.nodes == 1:
+        if self.fuse_qwz:
+            if g.nodes > 1:
+                Z.zpp_qgz_hop_reduce(1, self.msg1, self.msg1_scales, g.nodes, g.gpus_per_node,
+                                     g.bucket, g.block, g.bits, codes_out=self.msg2,
+                                     scales_out=self.msg2_scales, stream=stream)
+                if mark:
+                    mark("qgz_hop1")
+            hop, ci, si = (1, self.msg1, self.msg1_scales) if g.nodes == 1 else \
+                (2, self.msg2, self.msg2_scales)
+            Z.zpp_qgz_final_hop_adam_qwz(hop, ci, si, g.nodes, g.gpus_per_node, g.bucket, g.block,
+                                         g.bits, self.grad_out, adam, state, 8, self.w_codes[0],
+                                         self.w_scales[0], stream)
+            if mark:
+                mark("qgz_final_hop_qwz")
+        elif g.nodes == 1:
             Z.zpp_qgz_hop_reduce(1, self.msg1, self.msg1_scales, g.nodes, g.gpus_per_node,
                                  g.bucket, g.block, g.bits, grad_out=self.grad_out, adam=adam,
                                  state=state, stream=stream)

@@ -163,6 +163,32 @@ zpp_status zpp_qgz_hop_reduce(int32_t hop, const void* codes_in, const float* sc
                               const zpp_adam_hparams* adam, const zpp_adam_state* state,
                               void* stream);
 
+/* zpp_qgz_final_hop_adam_qwz -- the final hop of zpp_qgz_hop_reduce with the
+ * Adam step, fused with the int8 block quantization of the updated 16-bit
+ * parameters: the qwZ message of the next step's forward all-gather, produced
+ * without reading the parameters again.
+ * ("ZeRO-1/2/3", Stage 1 steps 6-7: the updated fp32 master is written back as
+ * 16-bit parameters, which the next all-gather distributes; "Quantized LLM
+ * Training at Scale with ZeRO++", 1 QWZ: that all-gather travels as blocks of
+ * 8-bit codes with one scale each.)
+ *   hop, codes_in .. grad_out, adam, state: as zpp_qgz_hop_reduce's final hop
+ *     (hop 1 with nodes == 1, else hop 2); adam and state are required,
+ *     state->param_bf16 may be NULL.
+ *   qwz_bits: 8.  The quantization block is `block`, restarting at every
+ *     rank's owned shard:
+ *   qwz_codes  [N_d][L] int8 (device, written), qwz_scales [N_d][L / block]
+ *     fp32 (device, written) -- exactly zpp_qwz_quant(param_bf16, N_d, L,
+ *     block, 8) of the new parameters.
+ * Requires L = bucket_elems / N_d to be a multiple of max(block, 512)
+ * (ZPP_ERR_UNSUPPORTED otherwise) and qwz_bits == 8 (ZPP_ERR_UNSUPPORTED for
+ * 4).  Other errors as zpp_qgz_hop_reduce. */
+zpp_status zpp_qgz_final_hop_adam_qwz(int32_t hop, const void* codes_in, const float* scales_in,
+                                      int32_t nodes, int32_t gpus_per_node,
+                                      int64_t bucket_elems, int32_t block, int32_t bits,
+                                      float* grad_out, const zpp_adam_hparams* adam,
+                                      const zpp_adam_state* state, int32_t qwz_bits,
+                                      void* qwz_codes, float* qwz_scales, void* stream);
+
 /* ---- sharded mixed-precision Adam ------------------------------------------ */
 
 /* zpp_shard_adam_step -- one Adam step on n owned parameters.

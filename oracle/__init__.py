@@ -271,3 +271,19 @@ def adam_step(g, master, m, v, lr, beta1, beta2, eps, t, want_param=True):
     _check(_load().orc_adam_step(_ptr(g), g.size, lr, beta1, beta2, eps, t, _ptr(master),
                                  _ptr(m), _ptr(v), _ptr(param)), "adam_step")
     return master, m, v, param
+
+
+# ---- next rows ---------------------------------------------------------------------
+
+def adam_then_qwz(g, master, m, v, lr, beta1, beta2, eps, t, nd: int, L: int, block: int,
+                  bits: int = 8):
+    """Adam step on every rank's owned slice, then the qwZ message of the new
+    16-bit parameters for the next forward all-gather ("ZeRO-1/2/3", Stage 1
+    steps 6-7: write back the 16-bit parameters, all-gather them; "Quantized
+    LLM Training at Scale with ZeRO++", 1 QWZ: that all-gather travels as
+    block-quantized 8-bit codes).  Element d*L + i is parameter i of rank d's
+    shard; blocks restart at every shard.
+    Returns (master, m, v, param_bf16_bits, codes, scales)."""
+    master, m, v, param = adam_step(g, master, m, v, lr, beta1, beta2, eps, t)
+    codes, scales = qwz_quant(param, nd, L, block, bits)
+    return master, m, v, param, codes, scales

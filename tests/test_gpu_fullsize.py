@@ -45,7 +45,7 @@ def sample_blocks(nblocks, k, seed):
     return sorted(picks)
 
 
-def build_path(Z, wl: W.Workload, keep_grad=True):
+def build_path(Z, wl: W.Workload, keep_grad=True, fuse_qwz=False):
     q, g = wl.qwz, wl.qgz
     qs = gs = None
     if q is not None:
@@ -54,7 +54,7 @@ def build_path(Z, wl: W.Workload, keep_grad=True):
         gs = Z.QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
     a = wl.adam
     adam = Z.AdamSpec(a.lr, a.beta1, a.beta2, a.eps, a.step) if (g and wl.fused_adam) else None
-    path = Z.CodecPath(qs, gs, adam, device="cuda", keep_grad=keep_grad)
+    path = Z.CodecPath(qs, gs, adam, device="cuda", keep_grad=keep_grad, fuse_qwz=fuse_qwz)
     if q is not None:
         synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, qs.phi, out=path.w)
     if g is not None:
@@ -166,6 +166,12 @@ def check_qgz(path, wl, nsample=2):
         assert_rel_close(gather_f32(path.m, gidx), wm, 1e-5, "m")
         assert_rel_close(gather_f32(path.v, gidx), wv, 1e-5, "v")
         assert_bf16_ulp(gather_u16(path.param, gidx), wb, "param")
+        if path.fuse_qwz:   # next step's weight message from the new parameters
+            wc, ws = oracle.qwz_quant(wb, Nd, Lm, B, 8)
+            got_c = gather_bytes(path.w_codes[0], gidx[::B], B).reshape(-1)
+            assert_bytes_equal(got_c, wc, "fused qwZ codes")
+            assert_f32_bitexact(gather_f32(path.w_scales[0], gidx[::B] // B), ws,
+                                "fused qwZ scales")
 
 
 @pytest.mark.parametrize("name", ["tiny", "llama", "two_hop", "7b"])
@@ -180,6 +186,21 @@ def test_workload_full_size(name):
         check_qwz(path, wl)
     if wl.qgz is not None:
         check_qgz(path, wl)
+    del path
+    torch.cuda.empty_cache()
+
+
+def test_llama_fused_adam_qwz_full_size():
+    """The llama step with the weights' qwZ message produced inside the final
+    hop's Adam pass (the owned slices are the qwZ shards)."""
+    Z = zpp()
+    wl = W.WORKLOADS["llama"]
+    torch.cuda.empty_cache()
+    path = build_path(Z, wl, fuse_qwz=True)
+    path.prime_fused_qwz()
+    path.run()
+    torch.cuda.synchronize()
+    check_qgz(path, wl)
     del path
     torch.cuda.empty_cache()
 

@@ -278,3 +278,66 @@ def test_tiny_workload_end_to_end():
                                        wl.adam.beta2, wl.adam.eps, wl.adam.step)
     assert_rel_close(np_f32(path.master), wp, 1e-5, "master")
     assert_bf16_ulp(u16(path.param), wpb, "param")
+
+
+# ---- next row: Adam -> qwZ of the new parameters, fused into the final hop -----------------------
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("N,G,block", [(1, 8, 512), (2, 2, 256), (2, 4, 1024), (4, 2, 2048),
+                                       (1, 4, 64), (2, 2, 4096)])
+def test_final_hop_adam_qwz(bits, N, G, block):
+    Z = zpp()
+    Nd = N * G
+    L = 3 * max(block, 512)
+    bucket = Nd * L
+    x = (RNG.standard_t(3, Nd * bucket) * 1e-3).astype(np.float32)
+    gb = oracle.f32_to_bf16(x)
+    c1, s1 = oracle.qgz_reorder_quant(gb, N, G, bucket, block, bits)
+    if N == 1:
+        gref = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
+        hop, ci, si = 1, torch.from_numpy(c1).cuda(), torch.from_numpy(s1).cuda()
+    else:
+        c2, s2 = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
+        gref = oracle.qgz_hop2(c2, s2, N, G, bucket, block, bits)
+        hop, ci, si = 2, torch.from_numpy(c2).cuda(), torch.from_numpy(s2).cuda()
+    p0 = (RNG.standard_normal(bucket) * 0.02).astype(np.float32)
+    m0 = (RNG.standard_normal(bucket) * 1e-4).astype(np.float32)
+    v0 = np.abs(RNG.standard_normal(bucket) * 1e-6).astype(np.float32)
+    hp = (1e-4, 0.9, 0.999, 1e-8, 4)
+    wp, wm, wv, wb, wc, ws = oracle.adam_then_qwz(gref, p0, m0, v0, *hp, Nd, L, block, 8)
+    master, m, v = (torch.from_numpy(a.copy()).cuda() for a in (p0, m0, v0))
+    param = torch.empty(bucket, dtype=torch.bfloat16, device="cuda")
+    grad = torch.full((bucket,), float("nan"), device="cuda")
+    qc = torch.full((bucket,), 0x5A, dtype=torch.uint8, device="cuda")
+    qs = torch.full((bucket // block,), float("nan"), device="cuda")
+    Z.zpp_qgz_final_hop_adam_qwz(hop, ci, si, N, G, bucket, block, bits, grad, hp,
+                                 (master, m, v, param), 8, qc, qs)
+    torch.cuda.synchronize()
+    assert_f32_bitexact(np_f32(grad), gref, "gradient")
+    assert_rel_close(np_f32(master), wp, 1e-5, "master")
+    assert_rel_close(np_f32(m), wm, 1e-5, "m")
+    assert_rel_close(np_f32(v), wv, 1e-5, "v")
+    assert_bf16_ulp(u16(param), wb, "param")
+    assert_bytes_equal(np_bytes(qc), wc, "fused qwZ codes")
+    assert_f32_bitexact(np_f32(qs), ws, "fused qwZ scales")
+
+
+def test_final_hop_adam_qwz_rejects_unsupported():
+    Z = zpp()
+    N, G, block, bits = 1, 4, 256, 4
+    bucket = 4 * 768                        # L = 768: not a multiple of 512
+    t = torch.zeros(bucket, device="cuda")
+    c = torch.zeros(bucket, dtype=torch.uint8, device="cuda")
+    st = (t, t.clone(), t.clone(), None)
+    with pytest.raises(Z.ZppError) as e:
+        Z.zpp_qgz_final_hop_adam_qwz(1, c, t, N, G, bucket, block, bits, None,
+                                     (1e-4, 0.9, 0.999, 1e-8, 1), st, 8, c, t)
+    assert e.value.status == Z.ZPP_ERR_UNSUPPORTED
+    bucket = 4 * 1024
+    t = torch.zeros(bucket, device="cuda")
+    c = torch.zeros(bucket, dtype=torch.uint8, device="cuda")
+    with pytest.raises(Z.ZppError) as e:
+        Z.zpp_qgz_final_hop_adam_qwz(1, c, t, N, G, bucket, block, bits, None,
+                                     (1e-4, 0.9, 0.999, 1e-8, 1), (t, t.clone(), t.clone(), None),
+                                     4, c, t)
+    assert e.value.status == Z.ZPP_ERR_UNSUPPORTED

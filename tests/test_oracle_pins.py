@@ -462,3 +462,27 @@ def test_block_quantization_beats_global(bits):
         e = accounting.quant_errors(x, 256, bits)
         assert e["block"]["rmse"] <= e["global"]["rmse"]
         assert e["rmse_ratio"] > 1.0
+
+
+# ---- next row: Adam -> qwZ of the new parameters ----------------------------------------------
+
+def test_adam_then_qwz_message_bounds_and_shard_restart():
+    nd, L, block = 4, 3 * 128, 128
+    n = nd * L
+    g = (RNG.standard_normal(n) * 1e-3).astype(np.float32)
+    p0 = (RNG.standard_normal(n) * 0.02).astype(np.float32)
+    p0[L - 1] = 5.0                      # a large weight at the end of rank 0's shard
+    z = np.zeros(n, np.float32)
+    master, m, v, param, codes, scales = oracle.adam_then_qwz(
+        g, p0, z, z, 1e-4, 0.9, 0.999, 1e-8, 1, nd, L, block)
+    pf = oracle.bf16_bits_to_f32(param).astype(np.float64)
+    nb = L // block
+    s = np.repeat(scales.astype(np.float64), block)
+    y = oracle.block_dequant(codes, scales, n, block, 8).astype(np.float64)
+    # the message dequantizes to within s/2 (plus rounding) of the new 16-bit parameters
+    assert np.all(np.abs(y - pf) <= s / 2 + 2 * 2.0 ** -24 * 128 * s)
+    # rank 0's last block sees the large weight, rank 1's first block does not
+    assert scales[nb - 1] >= np.float32(4.9 / 127)
+    assert scales[nb] < np.float32(0.2 / 127)
+    # the 16-bit parameters are the rounded masters of the Adam step
+    assert np.array_equal(param, oracle.f32_to_bf16(master))
