@@ -73,6 +73,8 @@ def _load():
         "orc_qgz_hop2": (I32, [P, P, I32, I32, I64, I64, I32, P]),
         "orc_adam_consts": (None, [F, F, I32, P, P, P, P]),
         "orc_adam_step": (I32, [P, I64, F, F, F, F, I32, P, P, P, P]),
+        "orc_grad_accumulate": (I32, [P, P, I64, I32]),
+        "orc_qgz_reorder_quant_f32": (I32, [P, I32, I32, I64, I64, I32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -287,3 +289,30 @@ def adam_then_qwz(g, master, m, v, lr, beta1, beta2, eps, t, nd: int, L: int, bl
     master, m, v, param = adam_step(g, master, m, v, lr, beta1, beta2, eps, t)
     codes, scales = qwz_quant(param, nd, L, block, bits)
     return master, m, v, param, codes, scales
+
+
+def grad_accumulate(microbatches_bf16) -> np.ndarray:
+    """fp32 sum of bf16 micro-batch gradients in arrival order (acc = g1;
+    acc = acc + gk) -- the accumulator before the reduce-scatter ("ZeRO Stage 2:
+    Gradient Partitioning", gradient accumulation)."""
+    mbs = [_c(g, np.uint16) for g in microbatches_bf16]
+    acc = np.zeros(mbs[0].size, dtype=np.float32)
+    for k, g in enumerate(mbs):
+        _check(_load().orc_grad_accumulate(_ptr(g), _ptr(acc), g.size, 1 if k == 0 else 0),
+               "grad_accumulate")
+    return acc
+
+
+def qgz_reorder_quant_f32(grads_f32, N: int, G: int, bucket: int, block: int, bits: int):
+    """The one-shot reorder + quantization of an fp32 bucket (accumulated gradients)."""
+    g = _c(grads_f32, np.float32)
+    Nd = N * G
+    assert g.size == Nd * bucket
+    if bits == 32:
+        codes = np.zeros(Nd * bucket, dtype=np.float32)
+    else:
+        codes = np.zeros(Nd * codes_bytes(bucket, bits), dtype=np.uint8)
+    scales = np.zeros(Nd * (bucket // block), dtype=np.float32)
+    _check(_load().orc_qgz_reorder_quant_f32(_ptr(g), N, G, bucket, block, bits, _ptr(codes),
+                                             _ptr(scales)), "qgz_reorder_quant_f32")
+    return codes, scales

@@ -242,10 +242,11 @@ static int qgz_check(int N, int G, int64_t bucket, int64_t block, int bits)
     return ORC_OK;
 }
 
-/* Same as orc_qgz_reorder_quant with an explicit permutation (perm[p] = j). */
-int orc_qgz_reorder_quant_perm(const uint16_t* grads, int N, int G, int64_t bucket,
-                               int64_t block, int bits, const int32_t* perm,
-                               void* codes, float* scales)
+/* Shared body: source element (r, i) read through either a bf16 or an fp32
+ * array (exactly one of g16 / g32 is non-NULL). */
+static int reorder_quant_src(const uint16_t* g16, const float* g32, int N, int G, int64_t bucket,
+                             int64_t block, int bits, const int32_t* perm, void* codes,
+                             float* scales)
 {
     if (qgz_check(N, G, bucket, block, bits)) return ORC_EINVAL;
     const int64_t Nd = (int64_t)N * G, L = bucket / Nd;
@@ -257,8 +258,10 @@ int orc_qgz_reorder_quant_perm(const uint16_t* grads, int N, int G, int64_t buck
         float* rs = scales ? scales + r * nb : NULL;
         for (int64_t p = 0; p < Nd; ++p) {
             int64_t j = perm[p];
-            for (int64_t i = 0; i < L; ++i)
-                tmp[i] = bf16_to_f32(grads[r * bucket + j * L + i]);
+            for (int64_t i = 0; i < L; ++i) {
+                const int64_t k = r * bucket + j * L + i;
+                tmp[i] = g16 ? bf16_to_f32(g16[k]) : g32[k];
+            }
             /* blocks of slice j restart at the slice start (L % block == 0) */
             for (int64_t b = 0; b < L / block; ++b)
                 quant_one_block(tmp + b * block, block, bits, rc, p * L + b * block,
@@ -267,6 +270,14 @@ int orc_qgz_reorder_quant_perm(const uint16_t* grads, int N, int G, int64_t buck
     }
     free(tmp);
     return ORC_OK;
+}
+
+/* Same as orc_qgz_reorder_quant with an explicit permutation (perm[p] = j). */
+int orc_qgz_reorder_quant_perm(const uint16_t* grads, int N, int G, int64_t bucket,
+                               int64_t block, int bits, const int32_t* perm,
+                               void* codes, float* scales)
+{
+    return reorder_quant_src(grads, NULL, N, G, bucket, block, bits, perm, codes, scales);
 }
 
 int orc_qgz_reorder_quant(const uint16_t* grads, int N, int G, int64_t bucket,
@@ -403,4 +414,34 @@ int orc_adam_step(const float* g, int64_t n, float lr, float beta1, float beta2,
         if (param) param[i] = orc_f32_to_bf16(p);
     }
     return ORC_OK;
+}
+
+/* ---- next row: gradient accumulation ---------------------------------------------
+ *
+ * ("ZeRO Stage 2: Gradient Partitioning", gradient accumulation: the partial
+ * gradients of several micro-batches are accumulated locally and the
+ * reduce-scatter fires once, when the accumulation is complete; the optimizer
+ * side holds them in fp32.)  Micro-batch gradients arrive in bf16 and are
+ * summed in fp32 in arrival order: acc = g_1; acc = acc + g_k.  The one-shot
+ * quantization of the accumulated bucket reads acc + g_last (one more fp32
+ * add) and is otherwise orc_qgz_reorder_quant on fp32 values. */
+
+int orc_grad_accumulate(const uint16_t* g, float* acc, int64_t n, int first)
+{
+    if (n < 0) return ORC_EINVAL;
+    for (int64_t i = 0; i < n; ++i)
+        acc[i] = first ? bf16_to_f32(g[i]) : acc[i] + bf16_to_f32(g[i]);
+    return ORC_OK;
+}
+
+int orc_qgz_reorder_quant_f32(const float* grads, int N, int G, int64_t bucket,
+                              int64_t block, int bits, void* codes, float* scales)
+{
+    if (N <= 0 || G <= 0) return ORC_EINVAL;
+    int32_t* perm = (int32_t*)malloc((size_t)N * G * sizeof(int32_t));
+    if (!perm) return ORC_EINVAL;
+    orc_qgz_slice_perm(N, G, perm);
+    int rc = reorder_quant_src(NULL, grads, N, G, bucket, block, bits, perm, codes, scales);
+    free(perm);
+    return rc;
 }

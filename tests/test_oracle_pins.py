@@ -486,3 +486,46 @@ def test_adam_then_qwz_message_bounds_and_shard_restart():
     assert scales[nb] < np.float32(0.2 / 127)
     # the 16-bit parameters are the rounded masters of the Adam step
     assert np.array_equal(param, oracle.f32_to_bf16(master))
+
+
+# ---- next row: gradient accumulation before the one-shot quantization ----------------------------
+
+def test_accumulation_of_exact_microbatches_equals_quantizing_the_sum():
+    """Small-integer micro-batches: the fp32 accumulation is exact, so
+    accumulate-then-quantize equals quantizing the exact (float64) sum, and the
+    identity codec returns the sum itself."""
+    N, G, block = 2, 2, 64
+    Nd, L = N * G, 2 * 64
+    bucket = Nd * L
+    mbs = [RNG.integers(-40, 41, size=Nd * bucket).astype(np.float32) for _ in range(5)]
+    acc = oracle.grad_accumulate([oracle.f32_to_bf16(m) for m in mbs])
+    exact = np.sum(np.stack(mbs).astype(np.float64), axis=0)
+    assert np.array_equal(acc.astype(np.float64), exact)
+    for bits in (8, 4):
+        c, s = oracle.qgz_reorder_quant_f32(acc, N, G, bucket, block, bits)
+        c2, s2 = oracle.qgz_reorder_quant_f32(exact.astype(np.float32), N, G, bucket, block, bits)
+        assert np.array_equal(c, c2) and np.array_equal(s, s2)
+    ident, _ = oracle.qgz_reorder_quant_f32(acc, N, G, bucket, L, 32)
+    perm = oracle.qgz_slice_perm(N, G)
+    x = exact.reshape(Nd, Nd, L)
+    assert np.array_equal(ident.reshape(Nd, Nd, L), x[:, perm, :].astype(np.float32))
+
+
+def test_accumulation_is_in_arrival_order():
+    """(2^24 + 1) - 2^24 = 0 in fp32 when the 1 comes second, 1 when it comes last."""
+    big, one = oracle.f32_to_bf16([2.0 ** 24]), oracle.f32_to_bf16([1.0])
+    nbig = oracle.f32_to_bf16([-(2.0 ** 24)])
+    assert oracle.grad_accumulate([big, one, nbig])[0] == 0.0
+    assert oracle.grad_accumulate([big, nbig, one])[0] == 1.0
+
+
+def test_bf16_bucket_quantizes_like_its_fp32_widening():
+    """The fp32-input quantizer on widened bf16 values equals the bf16 one."""
+    N, G, block = 2, 4, 128
+    Nd, L = N * G, 3 * 128
+    bucket = Nd * L
+    gb = oracle.f32_to_bf16((RNG.standard_normal(Nd * bucket) * 1e-3).astype(np.float32))
+    for bits in (8, 4):
+        a = oracle.qgz_reorder_quant(gb, N, G, bucket, block, bits)
+        b = oracle.qgz_reorder_quant_f32(oracle.bf16_bits_to_f32(gb), N, G, bucket, block, bits)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
