@@ -47,9 +47,14 @@ KERNEL_OF = {  # launch name -> CUDA kernel (for the roofline and the ncu summar
     "qgz_hop1": "hop_tiled_kernel<BITS, kRequant, LOGB>",
     "qgz_final_hop": "hop_tiled_kernel<BITS, kFinalAdam, LOGB>",
     "qgz_final_hop_qwz": "hop_tiled_kernel<BITS, kFinalAdamQwz, LOGB>",
+    "grad_accumulate": "accumulate_kernel",
+    "shard_adam": "adam_kernel<WIDE>",
+    "qgz_reorder_quant_acc": "quant_tiled_kernel<BITS, true, LOGB, true>",
 }
 KERNEL_SRC = {"qwz_quant": "quant.cu", "qwz_dequant": "quant.cu", "qgz_reorder_quant": "quant.cu",
-              "qgz_hop1": "hop.cu", "qgz_final_hop": "hop.cu", "qgz_final_hop_qwz": "hop.cu"}
+              "qgz_hop1": "hop.cu", "qgz_final_hop": "hop.cu", "qgz_final_hop_qwz": "hop.cu",
+              "grad_accumulate": "quant.cu", "qgz_reorder_quant_acc": "quant.cu",
+              "shard_adam": "adam.cu"}
 
 
 # ---- workload -> algorithmic bytes ------------------------------------------------
@@ -62,10 +67,13 @@ def msg_bytes(n, block, bits):
     return codes_bytes(n, bits) + 4 * (-(-n // block))
 
 
-def launch_bytes(wl, fuse_qwz=False):
+def launch_bytes(wl, fuse_qwz=False, microbatches=1):
     """[(launch name, algorithmic bytes)] of one pass, in launch order.  With
     fuse_qwz the weights' qwZ message is written by the final hop's Adam pass
-    (the next step's message), so the pass has no separate quantize launch."""
+    (the next step's message), so the pass has no separate quantize launch.
+    With M > 1 micro-batches, M-1 accumulate launches (bf16 in, fp32
+    accumulator read except the first, fp32 written) precede a one-shot
+    quantizer that reads the accumulator and the last micro-batch."""
     out = []
     q, g = wl.qwz, wl.qgz
     if q is not None and fuse_qwz:
@@ -82,7 +90,12 @@ def launch_bytes(wl, fuse_qwz=False):
     if g is not None:
         nd, b = g.nd, g.bucket
         m1 = nd * msg_bytes(b, g.block, g.bits)
-        out.append(("qgz_reorder_quant", 2 * nd * b + m1))
+        if microbatches > 1:
+            for k in range(microbatches - 1):
+                out.append(("grad_accumulate", (6 if k == 0 else 10) * nd * b))
+            out.append(("qgz_reorder_quant_acc", 6 * nd * b + m1))
+        else:
+            out.append(("qgz_reorder_quant", 2 * nd * b + m1))
         final_extra = (26 * b) if wl.fused_adam else 4 * b
         name = "qgz_final_hop"
         if fuse_qwz:
@@ -94,12 +107,18 @@ def launch_bytes(wl, fuse_qwz=False):
             m2 = nd * msg_bytes(g.nodes * g.slice_elems, g.block, g.bits)
             out.append(("qgz_hop1", m1 + m2))
             out.append((name, m2 + final_extra))
+    if wl.standalone_adam:   # g, master, m, v in; master, m, v, bf16 param out
+        out.append(("shard_adam", 30 * wl.standalone_adam))
     return out
 
 
-def workload_config(wl, name, fuse_qwz=False):
+def workload_config(wl, name, fuse_qwz=False, microbatches=1):
     q, g = wl.qwz, wl.qgz
     cfg = {"workload": wl.name, "name": name}
+    if microbatches > 1:
+        cfg["microbatches"] = microbatches
+        cfg["accumulation"] = ("fp32 accumulator over the first M-1 micro-batches; the one-shot "
+                               "quantizer adds the last")
     if fuse_qwz:
         cfg["qwz_fused"] = "the weights' int8 qwZ message is written by the final hop's Adam pass"
     if q is not None:
@@ -109,7 +128,9 @@ def workload_config(wl, name, fuse_qwz=False):
         cfg.update(N_d=g.nd, topology=f"{g.nodes}x{g.gpus_per_node}", bucket_per_rank=g.bucket,
                    qgz=f"int{g.bits} B={g.block}", adam="fused on the final hop" if wl.fused_adam
                    else "none")
-    per_step = sum(b for _, b in launch_bytes(wl, fuse_qwz))
+    if wl.standalone_adam:
+        cfg["standalone_adam_params"] = wl.standalone_adam
+    per_step = sum(b for _, b in launch_bytes(wl, fuse_qwz, microbatches))
     if per_step > 4 * L2_BYTES:
         cfg["l2"] = (f"inputs larger than L2: {per_step / 1e9:.2f} GB moved per step vs "
                      f"{L2_BYTES / 2**20:.0f} MiB L2; no flush")
@@ -240,13 +261,22 @@ def fill_inputs(path, wl):
         synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, path.qwz.phi, out=path.w, chunk=chunk)
     if wl.qgz is not None:
         g = wl.qgz
-        for r in range(g.nd):
-            synth.fill(g.grad, wl.seed, synth.grad_stream(r), 0, g.bucket,
-                       out=path.grads[r * g.bucket:(r + 1) * g.bucket], chunk=chunk)
+        for k, grads in enumerate(path.grads_mb):
+            for r in range(g.nd):
+                synth.fill(g.grad, wl.seed, synth.grad_stream(r, k), 0, g.bucket,
+                           out=grads[r * g.bucket:(r + 1) * g.bucket], chunk=chunk)
         if path.adam is not None:
             synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, g.bucket, out=path.param,
                        chunk=chunk)
             path.master.copy_(path.param.float())
+        if path.standalone_adam:
+            n = path.standalone_adam
+            t = synth.fill(W.GRAD_NORMAL, wl.seed, synth.SHARD_GRAD, 0, n, device=path.device,
+                           chunk=chunk)
+            path.sa_grad.copy_(t.float())
+            synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, g.bucket, n, out=t, chunk=chunk)
+            path.sa_master.copy_(t.float())
+            del t
     torch.cuda.synchronize()
 
 
@@ -262,12 +292,14 @@ def run_gpu(args, wl, rank, world, device):
     gs = Z.QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits) if g else None
     a = wl.adam
     adam = Z.AdamSpec(a.lr, a.beta1, a.beta2, a.eps, a.step) if (g and wl.fused_adam) else None
-    path = Z.CodecPath(qs, gs, adam, device=device, keep_grad=False, fuse_qwz=args.fuse_qwz)
+    path = Z.CodecPath(qs, gs, adam, device=device, keep_grad=False, fuse_qwz=args.fuse_qwz,
+                       microbatches=args.microbatches,
+                       standalone_adam=wl.standalone_adam if adam is not None else 0)
     fill_inputs(path, wl)
     stream = torch.cuda.current_stream(device)
     if args.fuse_qwz:
         path.prime_fused_qwz(stream)
-    lb = launch_bytes(wl, args.fuse_qwz)
+    lb = launch_bytes(wl, args.fuse_qwz, args.microbatches)
     step_bytes = sum(b for _, b in lb)
 
     def one_step(i, events=None):
@@ -334,7 +366,8 @@ def run_gpu(args, wl, rank, world, device):
                          "frac_of_peak": nb / (avg * 1e-3) / 1e9 / peak,
                          "share": sum(ts) / total_ms}
     dom = max(kernels, key=lambda k: kernels[k]["share"])
-    traffic = traffic_table().get((dom, args.config + ("+fuse_qwz" if args.fuse_qwz else "")))
+    traffic = traffic_table().get((dom, args.config + ("+fuse_qwz" if args.fuse_qwz else "")
+                                   + (f"+mb{args.microbatches}" if args.microbatches > 1 else "")))
     dk = kernels[dom]
     roofline = {"bound": "hbm", "kernel": dk["kernel"], "launch": dom,
                 "achieved": dk["gbs"], "peak": peak, "unit": "GB/s",
@@ -357,7 +390,7 @@ def run_gpu(args, wl, rank, world, device):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic: seeded counter-based generator (lowbias32 hash -> "
         "2^20-entry quantile table), weights N(0,0.02), grads per the workload",
-        "config": workload_config(wl, args.config, args.fuse_qwz),
+        "config": workload_config(wl, args.config, args.fuse_qwz, args.microbatches),
         "pct_hbm_peak_measured": 100.0 * value / world / peak,
         "pct_hbm_peak_nominal": 100.0 * value / world / NOMINAL_HBM_GBS,
         "qgz_bucket_elems_per_s": qgz_eps * world if qgz_eps else None,
@@ -375,19 +408,25 @@ def run_e2e(args, path, wl, stream, step_bytes, world, device):
     steps = max(3, min(args.steps, 30))
     # fused mode: the step's weight message comes from the previous step on the device
     w_host = path.w.cpu().pin_memory() if (path.qwz is not None and not path.fuse_qwz) else None
-    g_host = path.grads.cpu().pin_memory() if path.qgz is not None else None
+    g_host = [t.cpu().pin_memory() for t in path.grads_mb] if path.qgz is not None else None
     p_host = None
     if path.qgz is not None and path.adam is not None:
         p_host = torch.empty(path.qgz.bucket, dtype=torch.bfloat16).pin_memory()
+    sa_g = sa_p = None
+    if path.standalone_adam:
+        sa_g = path.sa_grad.cpu().pin_memory()
+        sa_p = torch.empty(path.standalone_adam, dtype=torch.bfloat16).pin_memory()
     for i in range(2):
-        path.run_from_host(w_host, g_host, p_host, stream, adam_step=1 + i)
+        path.run_from_host(w_host, g_host, p_host, stream, adam_step=1 + i, sa_grad_host=sa_g,
+                           sa_param_host=sa_p)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     h2d = d2h = 0
     for i in range(steps):
-        h2d, d2h = path.run_from_host(w_host, g_host, p_host, stream, adam_step=3 + i)
+        h2d, d2h = path.run_from_host(w_host, g_host, p_host, stream, adam_step=3 + i,
+                                      sa_grad_host=sa_g, sa_param_host=sa_p)
     torch.cuda.synchronize()
     dt = max_over_ranks((time.perf_counter() - t0) / steps, device)
     return {"value": whole_job_gbs(step_bytes, world, dt * 1e3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -402,9 +441,9 @@ class OracleSample:
     """A bounded sample of the workload for the CPU oracle: the first `nbw`
     blocks of every rank's weight shard (first qwZ call) and the first `nbg`
     blocks of every slice of every rank's bucket -- a self-contained smaller
-    instance of the same pass (same topology, block, bits, Adam)."""
+    instance of the same pass (same topology, block, bits, Adam, micro-batches)."""
 
-    def __init__(self, wl, nbw, nbg):
+    def __init__(self, wl, nbw, nbg, microbatches=1):
         import numpy as np
         import synth
         from synth import workloads as W
@@ -425,8 +464,10 @@ class OracleSample:
             Lm = nbg * g.block
             nd = g.nd
             pos = (np.arange(nd)[:, None] * g.slice_elems + np.arange(Lm)[None, :]).reshape(-1)
-            self.gx = np.concatenate([synth.bf16_to_u16(
-                synth.at(g.grad, wl.seed, synth.grad_stream(r), pos)) for r in range(nd)])
+            self.mbs = [np.concatenate([synth.bf16_to_u16(
+                synth.at(g.grad, wl.seed, synth.grad_stream(r, k), pos)) for r in range(nd)])
+                for k in range(microbatches)]
+            self.gx = self.mbs[-1]
             bucket = nd * Lm
             self.g = (g.nodes, g.gpus_per_node, bucket, g.block, g.bits)
             gidx = (np.arange(nd)[:, None] * g.slice_elems + np.arange(Lm)[None, :]).reshape(-1)
@@ -436,6 +477,9 @@ class OracleSample:
             self.zero = np.zeros(bucket, np.float32)
             m1 = nd * msg_bytes(bucket, g.block, g.bits)
             b = m1 + 2 * nd * bucket
+            if microbatches > 1:
+                b += 4 * nd * bucket + sum(6 if k == 0 else 10 for k in range(microbatches - 1)) \
+                    * nd * bucket
             if g.nodes == 1:
                 b += m1
             else:
@@ -444,6 +488,17 @@ class OracleSample:
             b += (26 if wl.fused_adam else 4) * bucket
             self.steps_bytes += b
             self.elems = nd * bucket
+        self.sa = None
+        if wl.standalone_adam and wl.fused_adam:   # a bounded slice of the standalone shard
+            n = min(wl.standalone_adam, max(4096, nbg * 2048))
+            t = synth.at(W.GRAD_NORMAL, wl.seed, synth.SHARD_GRAD, np.arange(n))
+            import oracle
+            self.sa = (oracle.bf16_bits_to_f32(synth.bf16_to_u16(t)),
+                       oracle.bf16_bits_to_f32(synth.bf16_to_u16(synth.at(
+                           W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS,
+                           np.arange(n) + (g.bucket if g is not None else 0)))),
+                       np.zeros(n, np.float32))
+            self.steps_bytes += 30 * n
 
     def run(self):
         import oracle
@@ -451,25 +506,37 @@ class OracleSample:
             c, s = oracle.qwz_quant(self.wx, *self.q)
             oracle.qwz_dequant(c, s, *self.q)
         if self.g is not None:
-            gr = oracle.qgz_reduce_scatter(self.gx, *self.g)
+            if len(self.mbs) > 1:
+                N = self.g[0]
+                c1, s1 = oracle.qgz_reorder_quant_f32(oracle.grad_accumulate(self.mbs), *self.g)
+                if N == 1:
+                    gr = oracle.qgz_hop1(c1, s1, *self.g)
+                else:
+                    gr = oracle.qgz_hop2(*oracle.qgz_hop1(c1, s1, *self.g), *self.g)
+            else:
+                gr = oracle.qgz_reduce_scatter(self.gx, *self.g)
             if self.wl.fused_adam:
                 a = self.wl.adam
                 oracle.adam_step(gr, self.master, self.zero, self.zero, a.lr, a.beta1, a.beta2,
                                  a.eps, a.step)
+        if self.sa is not None:
+            a = self.wl.adam
+            g, p, z = self.sa
+            oracle.adam_step(g, p, z, z, a.lr, a.beta1, a.beta2, a.eps, a.step)
 
 
-def sized_sample(wl, seconds):
+def sized_sample(wl, seconds, microbatches=1):
     """Calibrate the sample so one oracle pass takes about `seconds`."""
-    s = OracleSample(wl, 4, 2)
+    s = OracleSample(wl, 4, 2, microbatches)
     t = time.perf_counter()
     s.run()
     dt = max(time.perf_counter() - t, 1e-4)
     scale = max(1.0, seconds / dt)
-    return OracleSample(wl, int(4 * scale), int(2 * scale))
+    return OracleSample(wl, int(4 * scale), int(2 * scale), microbatches)
 
 
-def cpu_baseline(wl, seconds=12.0):
-    s = sized_sample(wl, seconds / 2)
+def cpu_baseline(wl, seconds=12.0, microbatches=1):
+    s = sized_sample(wl, seconds / 2, microbatches)
     t = time.perf_counter()
     n = 0
     while True:
@@ -489,7 +556,7 @@ def run_reference(args, wl):
     """The reference arm: the CPU oracle as it stands, on the host cores."""
     budget = 150.0
     per_step = max(0.2, min(5.0, budget / max(1, args.steps + args.warmup)))
-    s = sized_sample(wl, per_step)
+    s = sized_sample(wl, per_step, args.microbatches)
     for _ in range(args.warmup):
         s.run()
     t = time.perf_counter()
@@ -502,7 +569,7 @@ def run_reference(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded counter-based generator, bounded sample of the workload",
-        "config": workload_config(wl, args.config),
+        "config": workload_config(wl, args.config, microbatches=args.microbatches),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{s.steps_bytes / 1e6:.1f} MB of algorithmic traffic per "
                                    "step: the first blocks of every shard and slice of every "
@@ -621,6 +688,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fuse-qwz", action="store_true",
                     help="produce the weights' qwZ message inside the final hop's Adam pass")
+    ap.add_argument("--microbatches", type=int, default=1,
+                    help="gradient accumulation: micro-batches summed before the qgZ reduce")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="run the 144-point block/bits/topology/message-size sweep instead")
@@ -653,7 +722,7 @@ def main():
     try:
         res = run_gpu(args, wl, rank, world, device)
         if rank == 0 and world == 1 and not args.no_cpu:
-            res["cpu_baseline"] = cpu_baseline(wl)
+            res["cpu_baseline"] = cpu_baseline(wl, microbatches=args.microbatches)
         if rank == 0:
             print(json.dumps(res), flush=True)
     finally:

@@ -21,8 +21,8 @@ ZPP_OK, ZPP_ERR_INVALID_ARG, ZPP_ERR_MISALIGNED, ZPP_ERR_UNSUPPORTED, ZPP_ERR_CU
 
 # every symbol include/zpp.h declares
 EXPORTS = (
-    "zpp_qwz_quant", "zpp_qwz_dequant", "zpp_qgz_reorder_quant", "zpp_qgz_hop_reduce",
-    "zpp_qgz_final_hop_adam_qwz", "zpp_shard_adam_step", "zpp_codes_bytes", "zpp_num_blocks", "zpp_qgz_slice_perm",
+    "zpp_qwz_quant", "zpp_qwz_dequant", "zpp_qgz_reorder_quant", "zpp_grad_accumulate",
+    "zpp_qgz_reorder_quant_acc", "zpp_qgz_hop_reduce", "zpp_qgz_final_hop_adam_qwz", "zpp_shard_adam_step", "zpp_codes_bytes", "zpp_num_blocks", "zpp_qgz_slice_perm",
     "zpp_status_string", "zpp_last_cuda_error", "zpp_abi_version",
 )
 
@@ -68,6 +68,8 @@ def _lib():
         "zpp_qwz_quant": (I32, [P, I64, I64, I32, I32, P, P, P]),
         "zpp_qwz_dequant": (I32, [P, P, I64, I64, I32, I32, P, P]),
         "zpp_qgz_reorder_quant": (I32, [P, I32, I32, I64, I32, I32, P, P, P]),
+        "zpp_grad_accumulate": (I32, [P, P, I64, I32, P]),
+        "zpp_qgz_reorder_quant_acc": (I32, [P, P, I32, I32, I64, I32, I32, P, P, P]),
         "zpp_qgz_hop_reduce": (I32, [I32, P, P, I32, I32, I64, I32, I32, P, P, P, HP, ST, P]),
         "zpp_qgz_final_hop_adam_qwz": (I32, [I32, P, P, I32, I32, I64, I32, I32, P, HP, ST, I32, P,
                                               P, P]),
@@ -145,6 +147,23 @@ def zpp_qgz_reorder_quant(grads_bf16, nodes, gpus_per_node, bucket_elems, block,
                                         gpus_per_node, bucket_elems, block, bits,
                                         _dev(codes, _BYTES, "codes"), _dev(scales, _F32, "scales"),
                                         _stream(stream, grads_bf16)), "zpp_qgz_reorder_quant")
+
+
+def zpp_grad_accumulate(grads_bf16, acc, n, first, stream=None):
+    _check(_lib().zpp_grad_accumulate(_dev(grads_bf16, _BF16, "grads_bf16"), _dev(acc, _F32, "acc"),
+                                      n, int(first), _stream(stream, grads_bf16)),
+           "zpp_grad_accumulate")
+
+
+def zpp_qgz_reorder_quant_acc(grads_bf16, acc, nodes, gpus_per_node, bucket_elems, block, bits,
+                              codes, scales, stream=None):
+    _check(_lib().zpp_qgz_reorder_quant_acc(_dev(grads_bf16, _BF16, "grads_bf16"),
+                                            _dev(acc, _F32, "acc"), nodes, gpus_per_node,
+                                            bucket_elems, block, bits,
+                                            _dev(codes, _BYTES, "codes"),
+                                            _dev(scales, _F32, "scales"),
+                                            _stream(stream, grads_bf16)),
+           "zpp_qgz_reorder_quant_acc")
 
 
 def _adam_args(adam, state):

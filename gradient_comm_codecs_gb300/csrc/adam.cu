@@ -26,6 +26,8 @@ struct AdamArgs {
   AdamConsts ac;
 };
 
+// WIDE: g, master, m, v all 32-byte aligned; one 256-bit access per lane.
+template <bool WIDE>
 __global__ void __launch_bounds__(kThreads) adam_kernel(const AdamArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t units = (a.n + kAdamUnit - 1) / kAdamUnit;
@@ -37,15 +39,12 @@ __global__ void __launch_bounds__(kThreads) adam_kernel(const AdamArgs a) {
       AdamVec s[kAdamRows];
 #pragma unroll
       for (int k = 0; k < kAdamRows; ++k) {
-        const float4* gp = reinterpret_cast<const float4*>(a.g + base + k * 256);
-        const float4 g0 = __ldcs(gp), g1 = __ldcs(gp + 1);
-        g[k][0] = g0.x; g[k][1] = g0.y; g[k][2] = g0.z; g[k][3] = g0.w;
-        g[k][4] = g1.x; g[k][5] = g1.y; g[k][6] = g1.z; g[k][7] = g1.w;
-        s[k] = adam_load8(base + k * 256, a.master, a.m, a.v);
+        ld8_cs(a.g + base + k * 256, WIDE, g[k]);
+        s[k] = adam_load8(base + k * 256, a.master, a.m, a.v, WIDE);
       }
 #pragma unroll
       for (int k = 0; k < kAdamRows; ++k)
-        adam_apply8(g[k], s[k], base + k * 256, a.master, a.m, a.v, a.param, a.ac);
+        adam_apply8(g[k], s[k], base + k * 256, a.master, a.m, a.v, a.param, a.ac, WIDE);
     } else {
 #pragma unroll
       for (int k = 0; k < kAdamRows; ++k) {
@@ -70,8 +69,14 @@ cudaError_t launch_adam(const float* grad, int64_t n, const AdamConstsHost& ac, 
   AdamArgs a{grad, master, m, v, param, n,
              AdamConsts{ac.lr, ac.beta1, ac.beta2, ac.eps, ac.omb1, ac.omb2, ac.bc1, ac.bc2}};
   const int64_t units = (n + kAdamUnit - 1) / kAdamUnit;
-  const void* k = reinterpret_cast<const void*>(&adam_kernel);
-  adam_kernel<<<grid_for(k, (units + kWarps - 1) / kWarps), kThreads, 0, st>>>(a);
+  const int64_t ctas = (units + kWarps - 1) / kWarps;
+  if (aligned32(grad) && aligned32(master) && aligned32(m) && aligned32(v)) {
+    const void* k = reinterpret_cast<const void*>(&adam_kernel<true>);
+    adam_kernel<true><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+  } else {
+    const void* k = reinterpret_cast<const void*>(&adam_kernel<false>);
+    adam_kernel<false><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

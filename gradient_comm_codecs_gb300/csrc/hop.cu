@@ -40,6 +40,7 @@ struct HopArgs {
   uint16_t* param;
   uint8_t* qwz_codes;      // final hop + Adam + qwZ: next step's weight message
   float* qwz_scales;
+  bool wide;               // grad_out, master, m, v (those given) 32-byte aligned
 };
 
 // kFinalAdamQwz: the final hop, the Adam step, and the int8 block
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
     if constexpr (MODE == kFinalAdam) {
 #pragma unroll
       for (int k = 0; k < K; ++k)
-        if (on[k]) st[k] = adam_load8(obase + k * 256 + lane * 8, a.master, a.m, a.v);
+        if (on[k]) st[k] = adam_load8(obase + k * 256 + lane * 8, a.master, a.m, a.v, a.wide);
     }
 
     auto load = [&](CH& ch, int s0) {
@@ -193,13 +194,9 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
           g[i] = v.x;
           g[i + 1] = v.y;
         }
-        if (a.grad_out) {
-          float4* go = reinterpret_cast<float4*>(a.grad_out + idx);
-          __stcs(go, make_float4(g[0], g[1], g[2], g[3]));
-          __stcs(go + 1, make_float4(g[4], g[5], g[6], g[7]));
-        }
+        if (a.grad_out) st8_cs(a.grad_out + idx, a.wide, g);
         if constexpr (MODE == kFinalAdam)
-          adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac);
+          adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac, a.wide);
       }
     }
 
@@ -219,7 +216,11 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
 // per-element 64-bit address arithmetic and no tail predication.  Sources are
 // read two at a time, the next pair's loads in flight while the current pair
 // is summed.
-template <int BITS, int MODE, int LOGB>
+//
+// WIDE (fixed at compile time, so the loads of the next chunk schedule
+// freely around the state accesses): grad_out and the Adam state move as one
+// 256-bit access per lane; the launcher picks it when they are 32-byte aligned.
+template <int BITS, int MODE, int LOGB, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a) {
   using C = HopCfg<BITS, MODE, LOGB>;
   using G = typename C::G;
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
     AdamVec st[MODE >= kFinalAdam ? K : 1];
     if constexpr (MODE >= kFinalAdam) {
 #pragma unroll
-      for (int k = 0; k < K; ++k) st[k] = adam_load8(obase + k * 256 + lane * 8, a.master, a.m, a.v);
+      for (int k = 0; k < K; ++k) st[k] = adam_load8(obase + k * 256 + lane * 8, a.master, a.m, a.v, WIDE);
     }
     auto load = [&](CH& ch, int s0) {
 #pragma unroll
@@ -354,15 +355,11 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
           g[i] = v.x;
           g[i + 1] = v.y;
         }
-        if (a.grad_out) {
-          float4* go = reinterpret_cast<float4*>(a.grad_out + idx);
-          __stcs(go, make_float4(g[0], g[1], g[2], g[3]));
-          __stcs(go + 1, make_float4(g[4], g[5], g[6], g[7]));
-        }
+        if (a.grad_out) st8_cs(a.grad_out + idx, WIDE, g);
         if constexpr (MODE == kFinalAdam)
-          adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac);
+          adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac, WIDE);
         if constexpr (MODE == kFinalAdamQwz)
-          adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac, pq[k]);
+          adam_apply8(g, st[k], idx, a.master, a.m, a.v, a.param, a.ac, WIDE, pq[k]);
       }
       if constexpr (MODE == kFinalAdamQwz) {
         float am[K];
@@ -416,12 +413,16 @@ cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
     a.total_units = (int64_t)a.N * a.G * a.units_per_row;
     const int64_t groups = kWarps / C::WPB;
     const int64_t ctas = (a.total_units + groups - 1) / groups;
-    if (a.R % C::U == 0) {
-      const void* k = reinterpret_cast<const void*>(&hop_tiled_kernel<BITS, MODE, LOGB>);
-      hop_tiled_kernel<BITS, MODE, LOGB><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+    const bool tiled = a.R % C::U == 0;
+    if (tiled && (MODE == kRequant || a.wide)) {
+      constexpr bool W = MODE != kRequant;
+      const void* k = reinterpret_cast<const void*>(&hop_tiled_kernel<BITS, MODE, LOGB, W>);
+      hop_tiled_kernel<BITS, MODE, LOGB, W><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
     } else if constexpr (MODE == kFinalAdamQwz) {
-      return cudaErrorNotSupported;
-    } else {
+      if (!tiled) return cudaErrorNotSupported;
+      const void* k = reinterpret_cast<const void*>(&hop_tiled_kernel<BITS, MODE, LOGB, false>);
+      hop_tiled_kernel<BITS, MODE, LOGB, false><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+    } else {  // ragged rows, or fp32 arrays only 16-byte aligned
       const void* k = reinterpret_cast<const void*>(&hop_kernel<BITS, MODE, LOGB>);
       hop_kernel<BITS, MODE, LOGB><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
     }
@@ -456,6 +457,8 @@ cudaError_t launch_hop_reduce(const HopLaunch& h, cudaStream_t st) {
   a.param = h.param;
   a.qwz_codes = static_cast<uint8_t*>(h.qwz_codes);
   a.qwz_scales = h.qwz_scales;
+  a.wide = (!a.grad_out || aligned32(a.grad_out)) &&
+           (!h.adam || (aligned32(a.master) && aligned32(a.m) && aligned32(a.v)));
   const int b = h.block;
   if (!final_hop) return h.bits == 8 ? run_hop<8, kRequant>(a, b, st) : run_hop<4, kRequant>(a, b, st);
   if (h.adam && h.qwz_codes)

@@ -19,6 +19,7 @@ constexpr int kQRows = 4;  // rows of 256 elements per warp slab
 
 struct QuantArgs {
   const uint16_t* x;
+  const float* acc;       // accumulated micro-batch gradients (fp32), or null
   uint8_t* codes;
   float* scales;
   int64_t total_units;    // rows * units_per_row
@@ -29,18 +30,29 @@ struct QuantArgs {
   int32_t nd, N, G;       // qgZ topology
 };
 
-constexpr int kQStages = 4;  // units per warp in the shared-memory prefetch ring
-constexpr size_t kQSmem = (size_t)kWarps * kQStages * kQRows * 32 * sizeof(uint4);  // 64 KiB
+// A warp unit is q_rows rows of 256 elements; each warp keeps q_stages units
+// (a power of two) in a shared-memory prefetch ring.  bf16 input: 4 rows,
+// 4 stages (2 KiB a unit).  With the fp32 accumulator riding along (6 B an
+// element): 2 rows, 4 stages, so three 3 KiB units stay in flight per warp.
+template <bool ACC>
+__host__ __device__ constexpr int q_rows() { return ACC ? 2 : kQRows; }
+template <bool ACC>
+__host__ __device__ constexpr int q_stages() { return ACC ? 2 : 4; }
+template <bool ACC>
+__host__ __device__ constexpr size_t q_smem() {
+  return (size_t)kWarps * q_stages<ACC>() * q_rows<ACC>() * 32 *
+         (sizeof(uint4) + (ACC ? 2 * sizeof(float4) : 0));
+}
 
-// Quantize one warp's 1024 elements x[K][8] (lane-major rows of 256) whose
+// Quantize one warp's K*256 elements x[K][8] (lane-major rows of 256) whose
 // codes start at element `dst` of the code stream; every lane calls it.
 template <int BITS, int LOGB, class G>
-__device__ __forceinline__ void quantize_unit(float (&x)[kQRows][8], const int (&nv)[kQRows],
+__device__ __forceinline__ void quantize_unit(float (&x)[G::kRows][8], const int (&nv)[G::kRows],
                                               bool aligned, int64_t dst, int64_t scale0,
                                               int64_t e_warp, uint8_t* __restrict__ codes,
                                               float* __restrict__ scales, float (*red)[kWarps],
                                               int parity, int warp, int gid, int lane) {
-  constexpr int K = kQRows;
+  constexpr int K = G::kRows;
   constexpr int QMAX = (1 << (BITS - 1)) - 1;
   using CW = typename CodeVec<BITS>::T;
   float am[K];
@@ -90,34 +102,49 @@ __device__ __forceinline__ void quantize_unit(float (&x)[kQRows][8], const int (
 
 // Tiled layout: every row is a whole number of units, so unit u's input is the
 // contiguous run x[u*U + ...] (qwZ shards and qgZ slices follow one another in
-// memory).  Each warp keeps its next kQStages-1 units in flight with cp.async
+// memory).  Each warp keeps its next q_stages-1 units in flight with cp.async
 // into its own slice of shared memory: the loads never wait behind the
 // arithmetic and cost no registers.
 //
 // One row = one contiguous run quantized in blocks restarting at the row
 // start: a qwZ shard, or slice j of rank r's qgZ bucket, whose codes go to
 // slice position p = l'*N + n' (j = n'*G + l') of rank r's message.
-template <int BITS, bool REORDER, int LOGB>
+//
+// ACC: the quantized value is acc + x, the fp32 accumulator of the earlier
+// micro-batches plus the last micro-batch's bf16 gradient (one fp32 add).
+template <int BITS, bool REORDER, int LOGB, bool ACC>
 __global__ void __launch_bounds__(kThreads) quant_tiled_kernel(const QuantArgs a) {
-  using G = Geo<LOGB, kQRows>;
-  constexpr int K = kQRows, S = kQStages;
+  constexpr int K = q_rows<ACC>(), S = q_stages<ACC>();
+  using G = Geo<LOGB, K>;
   constexpr int GPC = kWarps / G::WPB;
   __shared__ float red[2][kWarps];
   extern __shared__ uint4 qsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = warp / G::WPB, wsub = warp - gid * G::WPB;
   uint4* ring = qsm + (size_t)warp * S * K * 32;  // [S][K][32]
+  float4* aring = reinterpret_cast<float4*>(qsm + (size_t)kWarps * S * K * 32) +
+                  (size_t)warp * S * K * 64;      // [S][K][64]: rows of 256 floats
 
   int64_t u, uend;
   unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
   if (u >= uend) return;  // the whole group shares the range
   const uint16_t* xg = a.x + (int64_t)wsub * G::kWarpElems + lane * 8;
+  const float* ag = ACC ? a.acc + (int64_t)wsub * G::kWarpElems + lane * 4 : nullptr;
   auto issue = [&](int64_t v) {
     if (v < uend) {
       const uint16_t* src = xg + v * G::U;
       uint4* slot = ring + (size_t)(v & (S - 1)) * K * 32 + lane;
 #pragma unroll
       for (int k = 0; k < K; ++k) cp_async16(slot + k * 32, src + k * 256);
+      if constexpr (ACC) {  // whole rows, 512 contiguous bytes per instruction
+        const float* asrc = ag + v * G::U;
+        float4* aslot = aring + (size_t)(v & (S - 1)) * K * 64 + lane;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          cp_async16(aslot + k * 64, asrc + k * 256);
+          cp_async16(aslot + k * 64 + 32, asrc + k * 256 + 128);
+        }
+      }
     }
     cp_async_commit();
   };
@@ -141,16 +168,30 @@ __global__ void __launch_bounds__(kThreads) quant_tiled_kernel(const QuantArgs a
       return row * a.row_len;
   };
   int64_t dst_row = row_dst();
-  const int nv[K] = {8, 8, 8, 8};
+  int nv[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) nv[k] = 8;
   int parity = 0;
 
   for (; u < uend; ++u, parity ^= 1) {
+    if constexpr (ACC) __syncwarp();  // every lane is done with the slot refilled next
     issue(u + S - 1);
     cp_async_wait<S - 1>();  // this unit's copies have landed
+    if constexpr (ACC) __syncwarp();  // ... the other lanes' accumulator copies too
     float x[K][8];
     const uint4* slot = ring + (size_t)(u & (S - 1)) * K * 32 + lane;
 #pragma unroll
     for (int k = 0; k < K; ++k) unpack_bf16x8(slot[k * 32], x[k]);
+    if constexpr (ACC) {
+      const float4* aslot = aring + (size_t)(u & (S - 1)) * K * 64 + 2 * lane;
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const float4 p0 = aslot[k * 64], p1 = aslot[k * 64 + 1];
+        const float av[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[k][i] = __fadd_rn(av[i], x[k][i]);
+      }
+    }
     const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;
     quantize_unit<BITS, LOGB, G>(x, nv, true, dst_row, dst_row >> LOGB, e_warp, a.codes, a.scales,
                                  red, parity, warp, gid, lane);
@@ -176,10 +217,10 @@ __global__ void __launch_bounds__(kThreads) quant_tiled_kernel(const QuantArgs a
 
 // General layout (a row tail shorter than a unit, or shards whose starts are
 // not 16-byte aligned): direct loads, element loads with zero fill where needed.
-template <int BITS, bool REORDER, int LOGB>
+template <int BITS, bool REORDER, int LOGB, bool ACC>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
-  using G = Geo<LOGB, kQRows>;
-  constexpr int K = kQRows;
+  constexpr int K = q_rows<ACC>();
+  using G = Geo<LOGB, K>;
   constexpr int GPC = kWarps / G::WPB;
   __shared__ float red[2][kWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -224,6 +265,12 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           x[k][i] = i < nv[k] ? __uint_as_float((uint32_t)xw[e + i] << 16) : 0.0f;
+      }
+      if constexpr (ACC) {
+        const float* aw = a.acc + src_base + e_warp + e;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < nv[k]) x[k][i] = __fadd_rn(aw[i], x[k][i]);
       }
     }
     quantize_unit<BITS, LOGB, G>(x, nv, aligned, dst_base, scale_base, e_warp, a.codes, a.scales,
@@ -327,25 +374,26 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) 
   }
 }
 
-template <int BITS, bool REORDER>
+template <int BITS, bool REORDER, bool ACC>
 cudaError_t run_quant(const QuantArgs& a0, int block, cudaStream_t st) {
   return dispatch_logb(block, [&](auto lb) -> cudaError_t {
     constexpr int LOGB = decltype(lb)::value;
-    using G = Geo<LOGB, kQRows>;
+    using G = Geo<LOGB, q_rows<ACC>()>;
     QuantArgs a = a0;
     a.units_per_row = (a.row_len + G::U - 1) / G::U;
     a.total_units = a.total_units * a.units_per_row;  // caller passes the row count
     const int64_t groups = kWarps / G::WPB;
     const int64_t ctas = (a.total_units + groups - 1) / groups;
     if (a.row_len % G::U == 0) {  // tiled: every unit full, 16-byte aligned
-      const void* k = reinterpret_cast<const void*>(&quant_tiled_kernel<BITS, REORDER, LOGB>);
+      constexpr size_t smem = q_smem<ACC>();
+      const void* k = reinterpret_cast<const void*>(&quant_tiled_kernel<BITS, REORDER, LOGB, ACC>);
       static const cudaError_t attr =
-          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmem);
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (attr != cudaSuccess) return attr;
-      quant_tiled_kernel<BITS, REORDER, LOGB><<<grid_for(k, ctas, kQSmem), kThreads, kQSmem, st>>>(a);
+      quant_tiled_kernel<BITS, REORDER, LOGB, ACC><<<grid_for(k, ctas, smem), kThreads, smem, st>>>(a);
     } else {
-      const void* k = reinterpret_cast<const void*>(&quant_kernel<BITS, REORDER, LOGB>);
-      quant_kernel<BITS, REORDER, LOGB><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+      const void* k = reinterpret_cast<const void*>(&quant_kernel<BITS, REORDER, LOGB, ACC>);
+      quant_kernel<BITS, REORDER, LOGB, ACC><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
     }
     return cudaGetLastError();
   });
@@ -362,7 +410,41 @@ cudaError_t run_dequant(const DequantArgs& a0, int block, cudaStream_t st) {
   });
 }
 
+// acc = (first ? 0 : acc) + (float)g for n elements; 8 per lane per step
+// (`wide`: acc 32-byte aligned, one 256-bit access per lane).
+__global__ void __launch_bounds__(kThreads) accumulate_kernel(const uint16_t* __restrict__ g,
+                                                              float* __restrict__ acc, int64_t n,
+                                                              int first, bool wide) {
+  const int64_t stride = (int64_t)gridDim.x * kThreads * 8;
+  for (int64_t i = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * 8; i < n; i += stride) {
+    if (i + 8 <= n) {
+      float x[8];
+      unpack_bf16x8(__ldcs(reinterpret_cast<const uint4*>(g + i)), x);
+      if (!first) {
+        float av[8];
+        ld8_cs(acc + i, wide, av);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = __fadd_rn(av[k], x[k]);
+      }
+      st8_cs(acc + i, wide, x);
+    } else {
+      for (int64_t k = i; k < n; ++k) {
+        const float x = __uint_as_float((uint32_t)g[k] << 16);
+        acc[k] = first ? x : __fadd_rn(acc[k], x);
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_grad_accumulate(const uint16_t* g, float* acc, int64_t n, int first,
+                                   cudaStream_t st) {
+  const void* k = reinterpret_cast<const void*>(&accumulate_kernel);
+  const int64_t ctas = (n + (int64_t)kThreads * 8 - 1) / ((int64_t)kThreads * 8);
+  accumulate_kernel<<<grid_for(k, ctas), kThreads, 0, st>>>(g, acc, n, first, aligned32(acc));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_qwz_quant(const uint16_t* x, int64_t nranks, int64_t shard, int32_t block,
                              int32_t bits, void* codes, float* scales, cudaStream_t st) {
@@ -373,12 +455,12 @@ cudaError_t launch_qwz_quant(const uint16_t* x, int64_t nranks, int64_t shard, i
   a.total_units = nranks;  // rows; scaled by units per row in run_quant
   a.row_len = shard;
   a.row_blocks = (shard + block - 1) / block;
-  return bits == 8 ? run_quant<8, false>(a, block, st) : run_quant<4, false>(a, block, st);
+  return bits == 8 ? run_quant<8, false, false>(a, block, st) : run_quant<4, false, false>(a, block, st);
 }
 
-cudaError_t launch_qgz_reorder_quant(const uint16_t* x, int32_t N, int32_t G, int64_t bucket,
-                                     int32_t block, int32_t bits, void* codes, float* scales,
-                                     cudaStream_t st) {
+cudaError_t launch_qgz_reorder_quant(const uint16_t* x, const float* acc, int32_t N, int32_t G,
+                                     int64_t bucket, int32_t block, int32_t bits, void* codes,
+                                     float* scales, cudaStream_t st) {
   QuantArgs a{};
   a.x = x;
   a.codes = static_cast<uint8_t*>(codes);
@@ -389,7 +471,9 @@ cudaError_t launch_qgz_reorder_quant(const uint16_t* x, int32_t N, int32_t G, in
   a.bucket = bucket;
   a.row_len = bucket / a.nd;
   a.total_units = (int64_t)a.nd * a.nd;  // rows (rank, slice)
-  return bits == 8 ? run_quant<8, true>(a, block, st) : run_quant<4, true>(a, block, st);
+  a.acc = acc;
+  if (acc) return bits == 8 ? run_quant<8, true, true>(a, block, st) : run_quant<4, true, true>(a, block, st);
+  return bits == 8 ? run_quant<8, true, false>(a, block, st) : run_quant<4, true, false>(a, block, st);
 }
 
 cudaError_t launch_qwz_dequant(const void* codes, const float* scales, int64_t nranks,

@@ -137,7 +137,7 @@ const char* zpp_status_string(zpp_status s) {
 
 const char* zpp_last_cuda_error(void) { return g_last_cuda_error; }
 
-int32_t zpp_abi_version(void) { return (1 << 16) | 0; }
+int32_t zpp_abi_version(void) { return (1 << 16) | 2; }
 
 zpp_status zpp_qwz_quant(const uint16_t* x_bf16, int64_t nranks, int64_t shard_elems,
                          int32_t block, int32_t bits, void* codes, float* scales,
@@ -176,7 +176,31 @@ zpp_status zpp_qgz_reorder_quant(const uint16_t* grads_bf16, int32_t nodes,
   if (!grads_bf16 || !codes || !scales) return ZPP_ERR_INVALID_ARG;
   if (!aligned16(grads_bf16) || !aligned16(codes) || !aligned16(scales))
     return ZPP_ERR_MISALIGNED;
-  return cuda_status(launch_qgz_reorder_quant(grads_bf16, nodes, gpus_per_node, bucket_elems,
+  return cuda_status(launch_qgz_reorder_quant(grads_bf16, nullptr, nodes, gpus_per_node,
+                                              bucket_elems, block, bits, codes, scales,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+zpp_status zpp_grad_accumulate(const uint16_t* grads_bf16, float* acc, int64_t n, int32_t first,
+                               void* stream) {
+  if (n < 0 || n > kMaxElems || (first != 0 && first != 1)) return ZPP_ERR_INVALID_ARG;
+  if (n == 0) return ZPP_OK;
+  if (!grads_bf16 || !acc) return ZPP_ERR_INVALID_ARG;
+  if (!aligned16(grads_bf16) || !aligned16(acc)) return ZPP_ERR_MISALIGNED;
+  return cuda_status(launch_grad_accumulate(grads_bf16, acc, n, first,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+zpp_status zpp_qgz_reorder_quant_acc(const uint16_t* grads_bf16, const float* acc, int32_t nodes,
+                                     int32_t gpus_per_node, int64_t bucket_elems, int32_t block,
+                                     int32_t bits, void* codes, float* scales, void* stream) {
+  zpp_status s = check_topology(nodes, gpus_per_node, bucket_elems, block, bits);
+  if (s != ZPP_OK) return s;
+  if (bucket_elems == 0) return ZPP_OK;
+  if (!grads_bf16 || !acc || !codes || !scales) return ZPP_ERR_INVALID_ARG;
+  if (!aligned16(grads_bf16) || !aligned16(acc) || !aligned16(codes) || !aligned16(scales))
+    return ZPP_ERR_MISALIGNED;
+  return cuda_status(launch_qgz_reorder_quant(grads_bf16, acc, nodes, gpus_per_node, bucket_elems,
                                               block, bits, codes, scales,
                                               static_cast<cudaStream_t>(stream)));
 }

@@ -20,9 +20,13 @@ struct AdamConstsHost {
 //          position p = (j % G) * N + j / G.
 cudaError_t launch_qwz_quant(const uint16_t* x, int64_t nranks, int64_t shard, int32_t block,
                              int32_t bits, void* codes, float* scales, cudaStream_t st);
-cudaError_t launch_qgz_reorder_quant(const uint16_t* x, int32_t N, int32_t G, int64_t bucket,
-                                     int32_t block, int32_t bits, void* codes, float* scales,
-                                     cudaStream_t st);
+// acc: null, or the fp32 accumulator of earlier micro-batches (quantizes acc + x).
+cudaError_t launch_qgz_reorder_quant(const uint16_t* x, const float* acc, int32_t N, int32_t G,
+                                     int64_t bucket, int32_t block, int32_t bits, void* codes,
+                                     float* scales, cudaStream_t st);
+// acc = (first ? 0 : acc) + (float)g, elementwise in fp32.
+cudaError_t launch_grad_accumulate(const uint16_t* g, float* acc, int64_t n, int first,
+                                   cudaStream_t st);
 cudaError_t launch_qwz_dequant(const void* codes, const float* scales, int64_t nranks,
                                int64_t shard, int32_t block, int32_t bits, uint16_t* y,
                                cudaStream_t st);

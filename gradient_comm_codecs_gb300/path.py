@@ -8,7 +8,12 @@ the C-ABI calls in order.  One pass (``CodecPath.run``) is
         chunks of a long weight tensor;
   qgZ   zpp_qgz_reorder_quant (every rank's bucket) -> zpp_qgz_hop_reduce(1)
         -> zpp_qgz_hop_reduce(2) when there is more than one node, the final
-        hop applying the Adam step to every rank's owned slice.
+        hop applying the Adam step to every rank's owned slice.  With M > 1
+        micro-batches the first M-1 are summed by zpp_grad_accumulate into an
+        fp32 accumulator and the one-shot quantizer reads accumulator + last
+        micro-batch (zpp_qgz_reorder_quant_acc).
+  Adam  optionally zpp_shard_adam_step over a further owned shard (the part
+        of a rank's parameters outside the reduced bucket).
 
 Every message between two calls is a separate HBM buffer, as the wire
 between two GPUs would be.
@@ -79,19 +84,28 @@ class CodecPath:
     """Buffers of one simulated ZeRO++ step on one device.
 
     Inputs the caller fills: ``w`` (bf16 weights, all calls concatenated),
-    ``grads`` (bf16 [N_d][bucket]) and the Adam state ``master, m, v``
+    ``grads`` (bf16 [N_d][bucket]; with micro-batches every tensor of
+    ``grads_mb``) and the Adam state ``master, m, v``
     (fp32 [bucket], element r*L + i owned by rank r).
     """
 
     def __init__(self, qwz: QwzSpec | None, qgz: QgzSpec | None, adam: AdamSpec | None,
                  device="cuda", keep_grad: bool = False, write_param: bool = True,
-                 fuse_qwz: bool = False):
-        """fuse_qwz: the weights' qwZ message is produced by the final hop's
+                 fuse_qwz: bool = False, microbatches: int = 1, standalone_adam: int = 0):
+        """standalone_adam: parameters of a separate owned shard stepped by
+        zpp_shard_adam_step after the reduce (fp32 ``sa_grad``, ``sa_master``,
+        ``sa_m``, ``sa_v``, bf16 ``sa_param``).
+        microbatches: gradients of that many micro-batches (``grads_mb``,
+        ``grads`` being the last) are accumulated before the reduce.
+        fuse_qwz: the weights' qwZ message is produced by the final hop's
         Adam pass from the new parameters (zpp_qgz_final_hop_adam_qwz) instead
         of a separate quantize call; needs the qwZ shards to be the ranks'
         owned qgZ slices (nranks = N_d, shard = L, same block, int8)."""
         self.qwz, self.qgz, self.adam = qwz, qgz, adam
         self.fuse_qwz = fuse_qwz
+        if microbatches < 1:
+            raise ValueError("microbatches must be >= 1")
+        self.microbatches = microbatches
         if fuse_qwz:
             ok = (qwz is not None and qgz is not None and adam is not None and qwz.bits == 8
                   and qwz.chunks == 1 and qwz.nranks == qgz.nd and qwz.shard == qgz.L
@@ -113,7 +127,10 @@ class CodecPath:
             self.launches_per_run += (1 if fuse_qwz else 2) * len(shards)
         if qgz is not None:
             nd, b = qgz.nd, qgz.bucket
-            self.grads = _empty(nd * b, torch.bfloat16, dev)
+            self.grads_mb = [_empty(nd * b, torch.bfloat16, dev) for _ in range(microbatches)]
+            self.grads = self.grads_mb[-1]
+            self.acc = _empty(nd * b, torch.float32, dev) if microbatches > 1 else None
+            self.launches_per_run += microbatches - 1
             self.msg1 = _empty(nd * Z.zpp_codes_bytes(b, qgz.bits), torch.uint8, dev)
             self.msg1_scales = _empty(nd * (b // qgz.block), torch.float32, dev)
             self.launches_per_run += 2
@@ -128,6 +145,17 @@ class CodecPath:
                 self.m = torch.zeros(b, dtype=torch.float32, device=dev)
                 self.v = torch.zeros(b, dtype=torch.float32, device=dev)
                 self.param = _empty(b, torch.bfloat16, dev) if write_param else None
+        self.standalone_adam = int(standalone_adam)
+        if self.standalone_adam:
+            if adam is None:
+                raise ValueError("standalone_adam needs the Adam hyper-parameters")
+            n = self.standalone_adam
+            self.sa_grad = _empty(n, torch.float32, dev)
+            self.sa_master = _empty(n, torch.float32, dev)
+            self.sa_m = torch.zeros(n, dtype=torch.float32, device=dev)
+            self.sa_v = torch.zeros(n, dtype=torch.float32, device=dev)
+            self.sa_param = _empty(n, torch.bfloat16, dev) if write_param else None
+            self.launches_per_run += 1
 
     # ---- the pass ---------------------------------------------------------------
     # `mark(name)`, when given, is called after each launch (the bench records a
@@ -163,10 +191,21 @@ class CodecPath:
 
     def run_qgz(self, stream=None, adam_step: int | None = None, mark=None):
         g = self.qgz
-        Z.zpp_qgz_reorder_quant(self.grads, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits,
-                                self.msg1, self.msg1_scales, stream)
-        if mark:
-            mark("qgz_reorder_quant")
+        if self.microbatches > 1:
+            n = g.nd * g.bucket
+            for k, gk in enumerate(self.grads_mb[:-1]):
+                Z.zpp_grad_accumulate(gk, self.acc, n, k == 0, stream)
+                if mark:
+                    mark("grad_accumulate")
+            Z.zpp_qgz_reorder_quant_acc(self.grads, self.acc, g.nodes, g.gpus_per_node, g.bucket,
+                                        g.block, g.bits, self.msg1, self.msg1_scales, stream)
+            if mark:
+                mark("qgz_reorder_quant_acc")
+        else:
+            Z.zpp_qgz_reorder_quant(self.grads, g.nodes, g.gpus_per_node, g.bucket, g.block,
+                                    g.bits, self.msg1, self.msg1_scales, stream)
+            if mark:
+                mark("qgz_reorder_quant")
         adam = state = None
         if self.adam is not None:
             hp = list(self.adam.hparams())
@@ -206,18 +245,31 @@ class CodecPath:
             if mark:
                 mark("qgz_final_hop")
 
+    def run_standalone_adam(self, stream=None, adam_step: int | None = None, mark=None):
+        hp = list(self.adam.hparams())
+        if adam_step is not None:
+            hp[4] = adam_step
+        Z.zpp_shard_adam_step(self.sa_grad, self.standalone_adam, tuple(hp),
+                              (self.sa_master, self.sa_m, self.sa_v, self.sa_param), stream)
+        if mark:
+            mark("shard_adam")
+
     def run(self, stream=None, adam_step: int | None = None, mark=None):
         if self.qwz is not None:
             self.run_qwz(stream, mark)
         if self.qgz is not None:
             self.run_qgz(stream, adam_step, mark)
+        if self.standalone_adam:
+            self.run_standalone_adam(stream, adam_step, mark)
 
     def run_from_host(self, w_host=None, grads_host=None, param_host=None, stream=None,
-                      adam_step: int | None = None):
+                      adam_step: int | None = None, sa_grad_host=None, sa_param_host=None):
         """One pass on host-resident data: copy this step's weights and
         gradients in (pinned host tensors, asynchronous on `stream`), run, and
-        copy the updated 16-bit parameters back.  Returns the bytes moved each
-        way (h2d, d2h)."""
+        copy the updated 16-bit parameters back.  `grads_host` is one tensor,
+        or one per micro-batch; `sa_grad_host`/`sa_param_host` are the
+        standalone shard's fp32 gradients in and bf16 parameters out.  Returns
+        the bytes moved each way (h2d, d2h)."""
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         h2d = d2h = 0
         with torch.cuda.stream(s):
@@ -225,11 +277,22 @@ class CodecPath:
                 self.w.copy_(w_host, non_blocking=True)
                 h2d += w_host.numel() * w_host.element_size()
             if grads_host is not None:
-                self.grads.copy_(grads_host, non_blocking=True)
-                h2d += grads_host.numel() * grads_host.element_size()
+                hosts = grads_host if isinstance(grads_host, (list, tuple)) else [grads_host]
+                if len(hosts) != self.microbatches:
+                    raise ValueError("grads_host: one tensor per micro-batch")
+                for dst, src in zip(self.grads_mb, hosts):
+                    dst.copy_(src, non_blocking=True)
+                    h2d += src.numel() * src.element_size()
+            if sa_grad_host is not None:
+                self.sa_grad.copy_(sa_grad_host, non_blocking=True)
+                h2d += sa_grad_host.numel() * sa_grad_host.element_size()
             self.run(s.cuda_stream, adam_step)
             if param_host is not None:
                 src = self.param if self.param is not None else self.master
                 param_host.copy_(src, non_blocking=True)
                 d2h += param_host.numel() * param_host.element_size()
+            if sa_param_host is not None:
+                src = self.sa_param if self.sa_param is not None else self.sa_master
+                sa_param_host.copy_(src, non_blocking=True)
+                d2h += sa_param_host.numel() * sa_param_host.element_size()
         return h2d, d2h

@@ -131,6 +131,33 @@ zpp_status zpp_qgz_reorder_quant(const uint16_t* grads_bf16, int32_t nodes,
                                  int32_t gpus_per_node, int64_t bucket_elems, int32_t block,
                                  int32_t bits, void* codes, float* scales, void* stream);
 
+/* zpp_grad_accumulate -- fp32 accumulation of one micro-batch's gradients.
+ * ("ZeRO Stage 2: Gradient Partitioning", compatibility with gradient
+ * accumulation: micro-batch gradients are summed on each GPU with no
+ * communication; the reduce-scatter runs once, after the last micro-batch.)
+ *   grads_bf16  [n] bf16 (device, read): this micro-batch's gradients.
+ *   acc         [n] fp32 (device, read unless first, written):
+ *               acc <- (first ? 0 : acc) + (float)grads, one fp32 add each.
+ *   first       1 for the first micro-batch (acc is not read), else 0.
+ * For the last micro-batch use zpp_qgz_reorder_quant_acc instead, which adds
+ * it while quantizing and never writes the sum back.
+ * Errors: ZPP_ERR_INVALID_ARG (n < 0, first not 0/1, NULL), ZPP_ERR_MISALIGNED. */
+zpp_status zpp_grad_accumulate(const uint16_t* grads_bf16, float* acc, int64_t n, int32_t first,
+                               void* stream);
+
+/* zpp_qgz_reorder_quant_acc -- zpp_qgz_reorder_quant of the accumulated
+ * gradient: element e of rank r's bucket is acc[r][e] + (float)grads[r][e]
+ * (one fp32 add, the last micro-batch's contribution), quantized from fp32.
+ * ("ZeRO Stage 2: Gradient Partitioning", gradient accumulation: the
+ * reduce-scatter fires once the accumulation is complete.)
+ *   grads_bf16  [N_d][bucket_elems] bf16 (device, read): the last micro-batch.
+ *   acc         [N_d][bucket_elems] fp32 (device, read): the earlier ones,
+ *               as zpp_grad_accumulate left them.
+ *   other arguments, layout and errors as zpp_qgz_reorder_quant. */
+zpp_status zpp_qgz_reorder_quant_acc(const uint16_t* grads_bf16, const float* acc, int32_t nodes,
+                                     int32_t gpus_per_node, int64_t bucket_elems, int32_t block,
+                                     int32_t bits, void* codes, float* scales, void* stream);
+
 /* zpp_qgz_hop_reduce -- one hop of the hierarchical all-to-all with reduction.
  * ("Quantized LLM Training at Scale with ZeRO++", 3 QGZ: first an intra-node
  * all-to-all and reduction, then an inter-node all-to-all; "ZeRO Stage 2:

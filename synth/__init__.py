@@ -37,7 +37,7 @@ import numpy as np
 import torch
 
 __all__ = [
-    "Dist", "Recipe", "WEIGHTS", "MOMENT_M", "MOMENT_V", "grad_stream",
+    "Dist", "Recipe", "WEIGHTS", "MOMENT_M", "MOMENT_V", "SHARD_GRAD", "grad_stream",
     "fill", "at", "hash32_int", "bf16_to_u16", "u16_to_bf16",
 ]
 
@@ -48,12 +48,14 @@ TABLE_BITS = 20
 WEIGHTS = 1
 MOMENT_M = 2
 MOMENT_V = 3
+SHARD_GRAD = 4   # gradients of an owned shard outside the reduced bucket
 _OUTLIER_SALT = 0x0D15EA5E
 
 
-def grad_stream(rank: int) -> int:
-    """Stream id of simulated data-parallel rank ``rank``'s gradient bucket."""
-    return 0x1000 + int(rank)
+def grad_stream(rank: int, microbatch: int = 0) -> int:
+    """Stream id of simulated data-parallel rank ``rank``'s gradient bucket
+    (of micro-batch ``microbatch`` when gradients are accumulated)."""
+    return 0x1000 + int(rank) + (int(microbatch) << 20)
 
 
 def hash32_int(x: int) -> int:

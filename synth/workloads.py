@@ -7,7 +7,9 @@ Input recipe (every workload): bf16 weights N(0, 0.02) from stream
 ``WEIGHTS`` indexed by global parameter index; the fp32 Adam master is the
 exact widening of those weights; m = v = 0 and step t = 1 unless a test says
 otherwise; rank r's gradient bucket comes from stream ``grad_stream(r)``
-indexed by position in the bucket.
+indexed by position in the bucket; a standalone Adam shard of n parameters
+has gradients N(0, 1e-3) from stream ``SHARD_GRAD`` and its master widened
+from the weights at global indices [bucket, bucket + n).
 """
 from __future__ import annotations
 

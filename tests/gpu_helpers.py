@@ -83,10 +83,11 @@ def gen_bf16(recipe, seed, stream, n, device="cpu"):
     return synth.fill(recipe, seed, stream, 0, n, device=device)
 
 
-def grads_for(qgz: W.QgZ, seed, device="cpu"):
-    """[N_d * bucket] bf16: rank r's bucket from grad_stream(r)."""
-    out = torch.empty(qgz.nd * qgz.bucket, dtype=torch.bfloat16, device=device)
+def grads_for(qgz: W.QgZ, seed, device="cpu", microbatch=0, out=None):
+    """[N_d * bucket] bf16: rank r's bucket from grad_stream(r, microbatch)."""
+    if out is None:
+        out = torch.empty(qgz.nd * qgz.bucket, dtype=torch.bfloat16, device=device)
     for r in range(qgz.nd):
-        synth.fill(qgz.grad, seed, synth.grad_stream(r), 0, qgz.bucket, device=device,
+        synth.fill(qgz.grad, seed, synth.grad_stream(r, microbatch), 0, qgz.bucket,
                    out=out[r * qgz.bucket:(r + 1) * qgz.bucket])
     return out

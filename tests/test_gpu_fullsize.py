@@ -45,7 +45,7 @@ def sample_blocks(nblocks, k, seed):
     return sorted(picks)
 
 
-def build_path(Z, wl: W.Workload, keep_grad=True, fuse_qwz=False):
+def build_path(Z, wl: W.Workload, keep_grad=True, fuse_qwz=False, microbatches=1):
     q, g = wl.qwz, wl.qgz
     qs = gs = None
     if q is not None:
@@ -54,11 +54,13 @@ def build_path(Z, wl: W.Workload, keep_grad=True, fuse_qwz=False):
         gs = Z.QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
     a = wl.adam
     adam = Z.AdamSpec(a.lr, a.beta1, a.beta2, a.eps, a.step) if (g and wl.fused_adam) else None
-    path = Z.CodecPath(qs, gs, adam, device="cuda", keep_grad=keep_grad, fuse_qwz=fuse_qwz)
+    path = Z.CodecPath(qs, gs, adam, device="cuda", keep_grad=keep_grad, fuse_qwz=fuse_qwz,
+                       microbatches=microbatches)
     if q is not None:
         synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, qs.phi, out=path.w)
     if g is not None:
-        path.grads.copy_(grads_for(g, wl.seed, device="cuda"))
+        for k, t in enumerate(path.grads_mb):
+            grads_for(g, wl.seed, microbatch=k, out=t)
         if adam is not None:
             m = synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, g.bucket, device="cuda")
             path.master.copy_(m.float())
@@ -108,11 +110,21 @@ def check_qgz(path, wl, nsample=2):
     # mini bucket: rank r, slice j, sampled block q
     pos = (np.arange(Nd)[:, None, None] * L + np.asarray(blocks)[None, :, None] * B
            + np.arange(B)[None, None, :]).reshape(-1)            # slice-relative index j*L + b*B + e
-    mini = np.empty(Nd * Nd * Lm, np.uint16)
-    for r in range(Nd):
-        mini[r * Nd * Lm:(r + 1) * Nd * Lm] = synth.bf16_to_u16(
-            synth.at(g.grad, wl.seed, synth.grad_stream(r), pos))
-    c1, s1 = oracle.qgz_reorder_quant(mini, N, G, Nd * Lm, B, bits)
+    mbs = []
+    for k in range(path.microbatches):
+        mini = np.empty(Nd * Nd * Lm, np.uint16)
+        for r in range(Nd):
+            mini[r * Nd * Lm:(r + 1) * Nd * Lm] = synth.bf16_to_u16(
+                synth.at(g.grad, wl.seed, synth.grad_stream(r, k), pos))
+        mbs.append(mini)
+    if len(mbs) == 1:
+        c1, s1 = oracle.qgz_reorder_quant(mbs[0], N, G, Nd * Lm, B, bits)
+    else:   # accumulated in arrival order, then quantized from fp32
+        acc = oracle.grad_accumulate(mbs)
+        c1, s1 = oracle.qgz_reorder_quant_f32(acc, N, G, Nd * Lm, B, bits)
+        wa = oracle.grad_accumulate(mbs[:-1])     # what the accumulator holds
+        aidx = (np.arange(Nd)[:, None] * bucket + pos[None, :]).reshape(-1)  # rank-major, as wa
+        assert_f32_bitexact(gather_f32(path.acc, aidx), wa, "accumulator")
     perm = oracle.qgz_slice_perm(N, G)
     cbr, cbm = oracle.codes_bytes(bucket, bits), oracle.codes_bytes(Nd * Lm, bits)
     bb = B * bits // 8
@@ -198,6 +210,22 @@ def test_llama_fused_adam_qwz_full_size():
     torch.cuda.empty_cache()
     path = build_path(Z, wl, fuse_qwz=True)
     path.prime_fused_qwz()
+    path.run()
+    torch.cuda.synchronize()
+    check_qgz(path, wl)
+    del path
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,microbatches", [("llama", 3), ("two_hop", 2)])
+def test_gradient_accumulation_full_size(name, microbatches):
+    """Gradient accumulation over micro-batches before the qgZ reduce: the
+    accumulator after M-1 micro-batches, the one-shot messages of the
+    accumulated bucket, the hops and the fused Adam on sampled blocks."""
+    Z = zpp()
+    wl = W.WORKLOADS[name]
+    torch.cuda.empty_cache()
+    path = build_path(Z, wl, microbatches=microbatches)
     path.run()
     torch.cuda.synchronize()
     check_qgz(path, wl)

@@ -280,6 +280,47 @@ def test_tiny_workload_end_to_end():
     assert_bf16_ulp(u16(path.param), wpb, "param")
 
 
+def test_codec_path_with_standalone_shard_and_microbatches():
+    """CodecPath with gradient accumulation over 3 micro-batches and a
+    standalone Adam shard (ragged size) after the reduce, two steps."""
+    Z = zpp()
+    from gradient_comm_codecs_gb300 import AdamSpec, CodecPath, QgzSpec
+    from gpu_helpers import grads_for
+    wl = W.TINY
+    g = wl.qgz
+    n_sa = 70001
+    path = CodecPath(None, QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits),
+                     AdamSpec(), device="cuda", keep_grad=True, microbatches=3,
+                     standalone_adam=n_sa)
+    mbs = [grads_for(g, wl.seed, microbatch=k) for k in range(3)]
+    for t, mb in zip(path.grads_mb, mbs):
+        t.copy_(mb)
+    master0 = synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, g.bucket).float()
+    path.master.copy_(master0)
+    sg = (RNG.standard_normal(n_sa) * 1e-3).astype(np.float32)
+    sp = (RNG.standard_normal(n_sa) * 0.02).astype(np.float32)
+    path.sa_grad.copy_(torch.from_numpy(sg))
+    path.sa_master.copy_(torch.from_numpy(sp))
+    acc = oracle.grad_accumulate([u16(t) for t in mbs])
+    c1, s1 = oracle.qgz_reorder_quant_f32(acc, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+    c2, s2 = oracle.qgz_hop1(c1, s1, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+    gref = oracle.qgz_hop2(c2, s2, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+    a = wl.adam
+    p, m, v = master0.numpy(), np.zeros(g.bucket, np.float32), np.zeros(g.bucket, np.float32)
+    q, qm, qv = sp, np.zeros(n_sa, np.float32), np.zeros(n_sa, np.float32)
+    for step in (1, 2):
+        path.run(adam_step=step)
+        torch.cuda.synchronize()
+        assert_f32_bitexact(np_f32(path.grad_out), gref, f"reduced gradient, step {step}")
+        p, m, v, pb = oracle.adam_step(gref, p, m, v, a.lr, a.beta1, a.beta2, a.eps, step)
+        q, qm, qv, qb = oracle.adam_step(sg, q, qm, qv, a.lr, a.beta1, a.beta2, a.eps, step)
+        assert_f32_bitexact(np_f32(path.master), p, f"master, step {step}")
+        assert_bf16_ulp(u16(path.param), pb, f"param, step {step}")
+        assert_f32_bitexact(np_f32(path.sa_master), q, f"standalone master, step {step}")
+        assert_f32_bitexact(np_f32(path.sa_v), qv, f"standalone v, step {step}")
+        assert_bf16_ulp(u16(path.sa_param), qb, f"standalone param, step {step}")
+
+
 # ---- next row: Adam -> qwZ of the new parameters, fused into the final hop -----------------------
 
 @pytest.mark.parametrize("bits", [4, 8])
@@ -341,3 +382,152 @@ def test_final_hop_adam_qwz_rejects_unsupported():
                                      (1e-4, 0.9, 0.999, 1e-8, 1), (t, t.clone(), t.clone(), None),
                                      4, c, t)
     assert e.value.status == Z.ZPP_ERR_UNSUPPORTED
+
+
+# ---- next row: gradient accumulation before the qgZ reduce --------------------------------------
+
+@pytest.mark.parametrize("n", [0, 1, 7, 8, 9, 2047, 123457])
+@pytest.mark.parametrize("M", [1, 2, 5])
+def test_grad_accumulate(n, M):
+    Z = zpp()
+    mbs = [oracle.f32_to_bf16((RNG.standard_t(3, n) * 1e-3).astype(np.float32)) for _ in range(M)]
+    acc = torch.full((max(n, 1),), float("nan"), device="cuda")[:n]
+    for k, g in enumerate(mbs):
+        Z.zpp_grad_accumulate(synth.u16_to_bf16(g).cuda(), acc, n, k == 0)
+    torch.cuda.synchronize()
+    if n:
+        assert_f32_bitexact(np_f32(acc), oracle.grad_accumulate(mbs), "accumulator")
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("block,slice_blocks", [(64, 19), (64, 16), (256, 5), (256, 8),
+                                                (1024, 3), (2048, 2), (4096, 1)])
+@pytest.mark.parametrize("N,G", [(1, 1), (1, 8), (2, 2), (2, 3), (4, 2)])
+@pytest.mark.parametrize("M", [2, 4])
+def test_qgz_reorder_quant_acc(bits, block, slice_blocks, N, G, M):
+    """One-shot messages of an accumulated bucket: the first M-1 micro-batches
+    through zpp_grad_accumulate, the last added inside the quantizer; then the
+    hops and the reduced gradient."""
+    Z = zpp()
+    Nd = N * G
+    bucket = Nd * slice_blocks * block
+    mbs = [oracle.f32_to_bf16((RNG.standard_t(3, Nd * bucket) * 1e-3).astype(np.float32))
+           for _ in range(M)]
+    if (N + G + M) % 2 == 0:    # the accumulated bucket exercises the quantizer's special cases
+        mbs[0] = oracle.f32_to_bf16(special_values(Nd * bucket, bits, block, RNG))
+        for k in range(1, M):
+            mbs[k] = np.zeros_like(mbs[0])
+    acc_ref = oracle.grad_accumulate(mbs)
+    c1, s1 = oracle.qgz_reorder_quant_f32(acc_ref, N, G, bucket, block, bits)
+    acc = torch.full((Nd * bucket,), float("nan"), device="cuda")
+    for k in range(M - 1):
+        Z.zpp_grad_accumulate(synth.u16_to_bf16(mbs[k]).cuda(), acc, Nd * bucket, k == 0)
+    torch.cuda.synchronize()
+    acc_before = acc.clone()
+    codes = torch.full((Nd * Z.zpp_codes_bytes(bucket, bits),), 0x5A, dtype=torch.uint8,
+                       device="cuda")
+    scales = torch.full((Nd * (bucket // block),), float("nan"), device="cuda")
+    Z.zpp_qgz_reorder_quant_acc(synth.u16_to_bf16(mbs[-1]).cuda(), acc, N, G, bucket, block, bits,
+                                codes, scales)
+    torch.cuda.synchronize()
+    assert torch.equal(acc.view(torch.int32), acc_before.view(torch.int32)), "acc was written"
+    assert_f32_bitexact(np_f32(acc), oracle.grad_accumulate(mbs[:-1]), "accumulator")
+    assert_bytes_equal(np_bytes(codes), c1, "one-shot codes of the accumulated bucket")
+    assert_f32_bitexact(np_f32(scales), s1, "one-shot scales of the accumulated bucket")
+    grad = torch.full((bucket,), float("nan"), device="cuda")
+    if N == 1:
+        Z.zpp_qgz_hop_reduce(1, codes, scales, N, G, bucket, block, bits, grad_out=grad)
+        want = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
+    else:
+        nl = bucket // G
+        c2 = torch.empty((Nd * Z.zpp_codes_bytes(nl, bits),), dtype=torch.uint8, device="cuda")
+        s2 = torch.empty((Nd * (nl // block),), device="cuda")
+        Z.zpp_qgz_hop_reduce(1, codes, scales, N, G, bucket, block, bits, codes_out=c2,
+                             scales_out=s2)
+        Z.zpp_qgz_hop_reduce(2, c2, s2, N, G, bucket, block, bits, grad_out=grad)
+        want = oracle.qgz_hop2(*oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits), N, G, bucket,
+                               block, bits)
+    torch.cuda.synchronize()
+    assert_f32_bitexact(np_f32(grad), want, "reduced gradient of the accumulated bucket")
+
+
+def test_accumulation_arguments():
+    Z = zpp()
+    g = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    acc = torch.zeros(65, device="cuda")
+    with pytest.raises(Z.ZppError) as e:
+        Z.zpp_grad_accumulate(g, acc, 64, 2)
+    assert e.value.status == Z.ZPP_ERR_INVALID_ARG
+    with pytest.raises(Z.ZppError) as e:
+        Z.zpp_grad_accumulate(g, acc[1:], 64, 1)
+    assert e.value.status == Z.ZPP_ERR_MISALIGNED
+    c = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(Z.ZppError) as e:   # bucket not a multiple of N_d * block
+        Z.zpp_qgz_reorder_quant_acc(g, acc, 1, 2, 64, 64, 8, c, acc)
+    assert e.value.status == Z.ZPP_ERR_INVALID_ARG
+    with pytest.raises(Z.ZppError) as e:
+        Z.zpp_qgz_reorder_quant_acc(g, acc[1:], 1, 1, 64, 64, 8, c, acc)
+    assert e.value.status == Z.ZPP_ERR_MISALIGNED
+
+
+# ---- fp32 arrays 16-byte but not 32-byte aligned (the two-128-bit access path) ------------------
+
+def _off16(a: np.ndarray) -> torch.Tensor:
+    """A device view of `a` starting 16 bytes into a fresh allocation."""
+    buf = torch.empty(a.size + 4, dtype=torch.float32, device="cuda")
+    buf[4:].copy_(torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)))
+    v = buf[4:]
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("N,G", [(1, 4), (2, 2)])
+def test_sixteen_byte_aligned_state(bits, N, G):
+    Z = zpp()
+    block = 256
+    Nd, L, bucket, gb = qgz_case(N, G, block, bits, 6, RNG)
+    want_g = oracle.qgz_reduce_scatter(gb, N, G, bucket, block, bits)
+    p0 = (RNG.standard_normal(bucket) * 0.02).astype(np.float32)
+    m0 = (RNG.standard_normal(bucket) * 1e-4).astype(np.float32)
+    v0 = np.abs(RNG.standard_normal(bucket) * 1e-6).astype(np.float32)
+    hp = (1e-4, 0.9, 0.999, 1e-8, 3)
+    wp, wm, wv, wb = oracle.adam_step(want_g, p0, m0, v0, *hp)
+    master, m, v = _off16(p0), _off16(m0), _off16(v0)
+    param = torch.empty(bucket, dtype=torch.bfloat16, device="cuda")
+    grad = _off16(np.full(bucket, np.nan, np.float32))
+    g = synth.u16_to_bf16(gb).cuda()
+    c1 = torch.empty(Nd * Z.zpp_codes_bytes(bucket, bits), dtype=torch.uint8, device="cuda")
+    s1 = torch.empty(Nd * (bucket // block), device="cuda")
+    Z.zpp_qgz_reorder_quant(g, N, G, bucket, block, bits, c1, s1)
+    if N == 1:
+        Z.zpp_qgz_hop_reduce(1, c1, s1, N, G, bucket, block, bits, grad_out=grad, adam=hp,
+                             state=(master, m, v, param))
+    else:
+        nl = N * L
+        c2 = torch.empty(Nd * Z.zpp_codes_bytes(nl, bits), dtype=torch.uint8, device="cuda")
+        s2 = torch.empty(Nd * (nl // block), device="cuda")
+        Z.zpp_qgz_hop_reduce(1, c1, s1, N, G, bucket, block, bits, codes_out=c2, scales_out=s2)
+        Z.zpp_qgz_hop_reduce(2, c2, s2, N, G, bucket, block, bits, grad_out=grad, adam=hp,
+                             state=(master, m, v, param))
+    torch.cuda.synchronize()
+    assert_f32_bitexact(np_f32(grad), want_g, "gradient")
+    assert_f32_bitexact(np_f32(master), wp, "master")
+    assert_f32_bitexact(np_f32(m), wm, "m")
+    assert_f32_bitexact(np_f32(v), wv, "v")
+    assert_bf16_ulp(u16(param), wb, "param")
+    # standalone Adam and accumulation on the same offset views
+    n = bucket - 3
+    gs = (RNG.standard_normal(n) * 1e-3).astype(np.float32)
+    wp2, wm2, wv2, _ = oracle.adam_step(gs, wp[:n], wm[:n], wv[:n], *hp)
+    Z.zpp_shard_adam_step(_off16(gs), n, hp, (master, m, v, None))
+    torch.cuda.synchronize()
+    assert_f32_bitexact(np_f32(master)[:n], wp2, "standalone master")
+    assert_f32_bitexact(np_f32(m)[:n], wm2, "standalone m")
+    assert_f32_bitexact(np_f32(v)[:n], wv2, "standalone v")
+    mbs = [gb[:n], gb[n:2 * n]]
+    acc = _off16(np.zeros(n, np.float32))
+    for k, mb in enumerate(mbs):
+        Z.zpp_grad_accumulate(synth.u16_to_bf16(mb).cuda(), acc, n, k == 0)
+    torch.cuda.synchronize()
+    assert_f32_bitexact(np_f32(acc), oracle.grad_accumulate(mbs), "accumulator")
