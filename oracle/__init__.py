@@ -75,6 +75,8 @@ def _load():
         "orc_adam_step": (I32, [P, I64, F, F, F, F, I32, P, P, P, P]),
         "orc_grad_accumulate": (I32, [P, P, I64, I32]),
         "orc_qgz_reorder_quant_f32": (I32, [P, I32, I32, I64, I64, I32, P, P]),
+        "orc_hpz_gather": (I32, [I32, I32, I64, I64, I32, P, P, P]),
+        "orc_hpz_secondary_bytes": (I64, [I32, I64, I64, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -316,3 +318,33 @@ def qgz_reorder_quant_f32(grads_f32, N: int, G: int, bucket: int, block: int, bi
     _check(_load().orc_qgz_reorder_quant_f32(_ptr(g), N, G, bucket, block, bits, _ptr(codes),
                                              _ptr(scales)), "qgz_reorder_quant_f32")
     return codes, scales
+
+
+def hpz_gather(secondaries, N: int, shard: int, block: int, bits: int) -> np.ndarray:
+    """Backward weight gather of one node under hpZ: `secondaries[l]` is local
+    rank l's secondary partition, (codes, scales) of N consecutive primary
+    shards, or a bf16 array of N*shard values when bits == 16.  Returns the
+    full bf16 weights [G*N*shard]."""
+    G = len(secondaries)
+    keep = []
+    cp = (ctypes.c_void_p * G)()
+    sp = (ctypes.c_void_p * G)()
+    for l, sec in enumerate(secondaries):
+        if bits == 16:
+            c = _c(sec, np.uint16)
+            s = None
+        else:
+            c, s = sec
+            c = np.ascontiguousarray(c)
+            s = _c(s, np.float32)
+        keep.append((c, s))
+        cp[l] = c.ctypes.data
+        sp[l] = None if s is None else s.ctypes.data
+    y = np.zeros(G * N * shard, dtype=np.uint16)
+    _check(_load().orc_hpz_gather(G, N, shard, block, bits, ctypes.cast(cp, ctypes.c_void_p),
+                                  ctypes.cast(sp, ctypes.c_void_p), _ptr(y)), "hpz_gather")
+    return y
+
+
+def hpz_secondary_bytes(N: int, shard: int, block: int, bits: int) -> int:
+    return int(_load().orc_hpz_secondary_bytes(N, shard, block, bits))

@@ -445,3 +445,42 @@ int orc_qgz_reorder_quant_f32(const float* grads, int N, int G, int64_t bucket,
     free(perm);
     return rc;
 }
+
+/* ---- hpZ: secondary partition and the node-local backward gather --------
+ * [P1] section 2 (HPZ): each node holds a secondary replica of the model
+ * partitions, so the backward weight gather reads only the node's own GPUs
+ * and its cross-node volume drops to zero.
+ * Reading: the secondary partition of rank (node n, local l) is slice l of
+ * the G-way split of the weights = the N consecutive primary shards
+ * l*N .. l*N + N - 1, kept in the form the forward all-gather delivered them
+ * (qwZ codes + scales; bf16 values when bits == 16).  The backward gather of
+ * node n concatenates the G secondary slices in local rank order
+ * l = 0..G-1 and dequantizes each shard as the forward receiver does. */
+
+int orc_hpz_gather(int G, int N, int64_t shard, int64_t block, int bits,
+                   const void* const* sec_codes, const float* const* sec_scales, uint16_t* y)
+{
+    if (G <= 0 || N <= 0 || shard < 0 || block <= 0) return ORC_EINVAL;
+    if (bits != 16 && bits != 8 && bits != 4) return ORC_EINVAL;
+    for (int l = 0; l < G; ++l) {
+        uint16_t* yl = y + (int64_t)l * N * shard;
+        if (bits == 16) {
+            const uint16_t* src = (const uint16_t*)sec_codes[l];
+            for (int64_t i = 0; i < (int64_t)N * shard; ++i) yl[i] = src[i];
+        } else {
+            int rc = orc_qwz_dequant(sec_codes[l], sec_scales[l], N, shard, block, bits, yl);
+            if (rc != ORC_OK) return rc;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Bytes one rank holds for its secondary partition: N shards' codes and
+ * scales (bits 4/8), or N shards of bf16 (bits 16). */
+int64_t orc_hpz_secondary_bytes(int N, int64_t shard, int64_t block, int bits)
+{
+    if (N <= 0 || shard < 0 || block <= 0) return -1;
+    if (bits == 16) return (int64_t)N * 2 * shard;
+    if (bits != 8 && bits != 4) return -1;
+    return (int64_t)N * (orc_codes_bytes(shard, bits) + 4 * orc_num_blocks(shard, block));
+}

@@ -529,3 +529,60 @@ def test_bf16_bucket_quantizes_like_its_fp32_widening():
         a = oracle.qgz_reorder_quant(gb, N, G, bucket, block, bits)
         b = oracle.qgz_reorder_quant_f32(oracle.bf16_bits_to_f32(gb), N, G, bucket, block, bits)
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---- next row: hpZ secondary partition and node-local backward gather ------------------------------
+
+def test_hpz_gather_hand_worked():
+    """G = 2 ranks, N = 2 shards each, shard = 4, block = 2, int8: the
+    gathered weights are q * s for hand-picked codes and power-of-two scales."""
+    codes = [np.array([1, -2, 3, 4, -5, 6, 7, -8], np.int8).view(np.uint8),
+             np.array([10, 0, -1, 2, 127, -127, 64, 32], np.int8).view(np.uint8)]
+    scales = [np.array([0.5, 0.25, 1.0, 2.0], np.float32),
+              np.array([0.125, 4.0, 2.0 ** -7, 1.0], np.float32)]
+    y = oracle.hpz_gather(list(zip(codes, scales)), 2, 4, 2, 8)
+    want = [0.5, -1.0, 0.75, 1.0, -5.0, 6.0, 14.0, -16.0,
+            1.25, 0.0, -4.0, 8.0, 127 / 128, -127 / 128, 64.0, 32.0]
+    assert np.array_equal(oracle.bf16_bits_to_f32(y), np.array(want, np.float32))
+
+
+@pytest.mark.parametrize("bits", [8, 4, 16])
+@pytest.mark.parametrize("N,G", [(1, 8), (2, 4), (4, 2), (3, 3)])
+def test_hpz_gather_of_kept_forward_messages_is_the_forward_gather(bits, N, G):
+    """The secondary partitions are the forward all-gather's messages of the
+    node's slices; gathering them in local rank order rebuilds exactly the
+    weights the forward all-gather delivered, and a swap of two ranks'
+    secondaries shows in the result."""
+    Nd, shard, block = N * G, 3 * 256 + 64, 128
+    w = oracle.f32_to_bf16((RNG.standard_normal(Nd * shard) * 0.02).astype(np.float32))
+    if bits == 16:
+        fwd = w
+        secs = [w[l * N * shard:(l + 1) * N * shard].copy() for l in range(G)]
+    else:
+        c, s = oracle.qwz_quant(w, Nd, shard, block, bits)
+        fwd = oracle.qwz_dequant(c, s, Nd, shard, block, bits)
+        cb, nb = oracle.codes_bytes(shard, bits), oracle.num_blocks(shard, block)
+        secs = [(c[l * N * cb:(l + 1) * N * cb].copy(), s[l * N * nb:(l + 1) * N * nb].copy())
+                for l in range(G)]
+    y = oracle.hpz_gather(secs, N, shard, block, bits)
+    assert np.array_equal(y, fwd)
+    if G > 1:
+        secs[0], secs[1] = secs[1], secs[0]
+        assert not np.array_equal(oracle.hpz_gather(secs, N, shard, block, bits), fwd)
+
+
+def test_hpz_secondary_memory_is_a_node_replica():
+    """Each rank keeps Phi/G of the weights (codes + scales); the G ranks of a
+    node together hold one full replica, the memory the pages trade for the
+    zero cross-node backward volume."""
+    for N, G in ((1, 8), (2, 8), (8, 8), (16, 8)):
+        Nd = N * G
+        for block, bits in ((256, 8), (2048, 8), (512, 4)):
+            shard = 64 * block
+            phi = Nd * shard
+            per_rank = oracle.hpz_secondary_bytes(N, shard, block, bits)
+            assert per_rank == Fraction(phi, G) * Fraction(bits, 8) + 4 * Fraction(phi, G * block)
+            assert G * per_rank == accounting.quantized_bytes(phi, block, bits)
+            assert oracle.hpz_secondary_bytes(N, shard, block, 16) == 2 * phi // G
+    gv = golden("zeropp_volume.txt")
+    assert Fraction(gv["hpz_bwd_cross_node_M"]) == 0
