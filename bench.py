@@ -49,12 +49,13 @@ KERNEL_OF = {  # launch name -> CUDA kernel (for the roofline and the ncu summar
     "qgz_final_hop_qwz": "hop_tiled_kernel<BITS, kFinalAdamQwz, LOGB>",
     "grad_accumulate": "accumulate_kernel",
     "shard_adam": "adam_kernel<WIDE>",
+    "hpz_gather": "dequant_kernel<BITS, LOGB> (G secondary sources)",
     "qgz_reorder_quant_acc": "quant_tiled_kernel<BITS, true, LOGB, true>",
 }
 KERNEL_SRC = {"qwz_quant": "quant.cu", "qwz_dequant": "quant.cu", "qgz_reorder_quant": "quant.cu",
               "qgz_hop1": "hop.cu", "qgz_final_hop": "hop.cu", "qgz_final_hop_qwz": "hop.cu",
               "grad_accumulate": "quant.cu", "qgz_reorder_quant_acc": "quant.cu",
-              "shard_adam": "adam.cu"}
+              "shard_adam": "adam.cu", "hpz_gather": "quant.cu"}
 
 
 # ---- workload -> algorithmic bytes ------------------------------------------------
@@ -67,13 +68,15 @@ def msg_bytes(n, block, bits):
     return codes_bytes(n, bits) + 4 * (-(-n // block))
 
 
-def launch_bytes(wl, fuse_qwz=False, microbatches=1):
+def launch_bytes(wl, fuse_qwz=False, microbatches=1, hpz=False):
     """[(launch name, algorithmic bytes)] of one pass, in launch order.  With
     fuse_qwz the weights' qwZ message is written by the final hop's Adam pass
     (the next step's message), so the pass has no separate quantize launch.
     With M > 1 micro-batches, M-1 accumulate launches (bf16 in, fp32
     accumulator read except the first, fp32 written) precede a one-shot
-    quantizer that reads the accumulator and the last micro-batch."""
+    quantizer that reads the accumulator and the last micro-batch.  With hpz
+    the backward gather reads the node's secondary partitions (the whole
+    message) and writes the bf16 weights again."""
     out = []
     q, g = wl.qwz, wl.qgz
     if q is not None and fuse_qwz:
@@ -87,6 +90,9 @@ def launch_bytes(wl, fuse_qwz=False, microbatches=1):
             m = q.nranks * msg_bytes(s, q.block, q.bits)
             out.append(("qwz_quant", 2 * q.nranks * s + m))
             out.append(("qwz_dequant", m + 2 * q.nranks * s))
+    if q is not None and hpz:
+        out.append(("hpz_gather", q.nranks * msg_bytes(q.shard, q.block, q.bits)
+                    + 2 * q.nranks * q.shard))
     if g is not None:
         nd, b = g.nd, g.bucket
         m1 = nd * msg_bytes(b, g.block, g.bits)
@@ -112,9 +118,12 @@ def launch_bytes(wl, fuse_qwz=False, microbatches=1):
     return out
 
 
-def workload_config(wl, name, fuse_qwz=False, microbatches=1):
+def workload_config(wl, name, fuse_qwz=False, microbatches=1, hpz=False):
     q, g = wl.qwz, wl.qgz
     cfg = {"workload": wl.name, "name": name}
+    if hpz:
+        cfg["hpz"] = ("backward weight gather from the node's secondary partitions "
+                      f"({hpz_nodes(wl)} node(s) x {q.nranks // hpz_nodes(wl)} GPUs)")
     if microbatches > 1:
         cfg["microbatches"] = microbatches
         cfg["accumulation"] = ("fp32 accumulator over the first M-1 micro-batches; the one-shot "
@@ -130,7 +139,7 @@ def workload_config(wl, name, fuse_qwz=False, microbatches=1):
                    else "none")
     if wl.standalone_adam:
         cfg["standalone_adam_params"] = wl.standalone_adam
-    per_step = sum(b for _, b in launch_bytes(wl, fuse_qwz, microbatches))
+    per_step = sum(b for _, b in launch_bytes(wl, fuse_qwz, microbatches, hpz))
     if per_step > 4 * L2_BYTES:
         cfg["l2"] = (f"inputs larger than L2: {per_step / 1e9:.2f} GB moved per step vs "
                      f"{L2_BYTES / 2**20:.0f} MiB L2; no flush")
@@ -139,6 +148,14 @@ def workload_config(wl, name, fuse_qwz=False, microbatches=1):
                      f"{L2_BYTES / 2**20:.0f} MiB L2; not a roofline configuration")
     cfg["arithmetic"] = "bf16 in, int8/int4 codes + fp32 scales, fp32 sums and Adam"
     return cfg
+
+
+def hpz_nodes(wl):
+    """hpZ node count of the qwZ ranks: the qgZ topology's when they coincide."""
+    q, g = wl.qwz, wl.qgz
+    if g is not None and q.nranks == g.nd:
+        return g.nodes
+    return 1
 
 
 def measured_peak():
@@ -287,19 +304,20 @@ def run_gpu(args, wl, rank, world, device):
     _build.build()
 
     q, g = wl.qwz, wl.qgz
-    qs = Z.QwzSpec(q.nranks, q.shard, q.block, q.bits, chunks=q.calls,
-                   tail_shard=q.tail_shard) if q else None
+    qs = Z.QwzSpec(q.nranks, q.shard, q.block, q.bits, chunks=q.calls, tail_shard=q.tail_shard,
+                   nodes=hpz_nodes(wl) if args.hpz else 1) if q else None
     gs = Z.QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits) if g else None
     a = wl.adam
     adam = Z.AdamSpec(a.lr, a.beta1, a.beta2, a.eps, a.step) if (g and wl.fused_adam) else None
     path = Z.CodecPath(qs, gs, adam, device=device, keep_grad=False, fuse_qwz=args.fuse_qwz,
                        microbatches=args.microbatches,
-                       standalone_adam=wl.standalone_adam if adam is not None else 0)
+                       standalone_adam=wl.standalone_adam if adam is not None else 0,
+                       hpz=args.hpz)
     fill_inputs(path, wl)
     stream = torch.cuda.current_stream(device)
     if args.fuse_qwz:
         path.prime_fused_qwz(stream)
-    lb = launch_bytes(wl, args.fuse_qwz, args.microbatches)
+    lb = launch_bytes(wl, args.fuse_qwz, args.microbatches, args.hpz)
     step_bytes = sum(b for _, b in lb)
 
     def one_step(i, events=None):
@@ -367,7 +385,8 @@ def run_gpu(args, wl, rank, world, device):
                          "share": sum(ts) / total_ms}
     dom = max(kernels, key=lambda k: kernels[k]["share"])
     traffic = traffic_table().get((dom, args.config + ("+fuse_qwz" if args.fuse_qwz else "")
-                                   + (f"+mb{args.microbatches}" if args.microbatches > 1 else "")))
+                                   + (f"+mb{args.microbatches}" if args.microbatches > 1 else "")
+                                   + ("+hpz" if args.hpz else "")))
     dk = kernels[dom]
     roofline = {"bound": "hbm", "kernel": dk["kernel"], "launch": dom,
                 "achieved": dk["gbs"], "peak": peak, "unit": "GB/s",
@@ -390,7 +409,7 @@ def run_gpu(args, wl, rank, world, device):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic: seeded counter-based generator (lowbias32 hash -> "
         "2^20-entry quantile table), weights N(0,0.02), grads per the workload",
-        "config": workload_config(wl, args.config, args.fuse_qwz, args.microbatches),
+        "config": workload_config(wl, args.config, args.fuse_qwz, args.microbatches, args.hpz),
         "pct_hbm_peak_measured": 100.0 * value / world / peak,
         "pct_hbm_peak_nominal": 100.0 * value / world / NOMINAL_HBM_GBS,
         "qgz_bucket_elems_per_s": qgz_eps * world if qgz_eps else None,
@@ -443,7 +462,7 @@ class OracleSample:
     blocks of every slice of every rank's bucket -- a self-contained smaller
     instance of the same pass (same topology, block, bits, Adam, micro-batches)."""
 
-    def __init__(self, wl, nbw, nbg, microbatches=1):
+    def __init__(self, wl, nbw, nbg, microbatches=1, hpz=False):
         import numpy as np
         import synth
         from synth import workloads as W
@@ -459,6 +478,9 @@ class OracleSample:
             self.q = (q.nranks, n, q.block, q.bits)
             m = q.nranks * msg_bytes(n, q.block, q.bits)
             self.steps_bytes += 2 * (2 * q.nranks * n + m)
+            self.hpz = hpz_nodes(wl) if hpz else 0
+            if hpz:
+                self.steps_bytes += 2 * q.nranks * n + m
         if g is not None:
             nbg = max(1, min(nbg, g.slice_elems // g.block))
             Lm = nbg * g.block
@@ -505,6 +527,12 @@ class OracleSample:
         if self.q is not None:
             c, s = oracle.qwz_quant(self.wx, *self.q)
             oracle.qwz_dequant(c, s, *self.q)
+            if self.hpz:
+                nr, n, block, bits = self.q
+                N, G = self.hpz, nr // self.hpz
+                cb, nb = oracle.codes_bytes(n, bits), oracle.num_blocks(n, block)
+                oracle.hpz_gather([(c[l * N * cb:(l + 1) * N * cb], s[l * N * nb:(l + 1) * N * nb])
+                                   for l in range(G)], N, n, block, bits)
         if self.g is not None:
             if len(self.mbs) > 1:
                 N = self.g[0]
@@ -525,18 +553,18 @@ class OracleSample:
             oracle.adam_step(g, p, z, z, a.lr, a.beta1, a.beta2, a.eps, a.step)
 
 
-def sized_sample(wl, seconds, microbatches=1):
+def sized_sample(wl, seconds, microbatches=1, hpz=False):
     """Calibrate the sample so one oracle pass takes about `seconds`."""
-    s = OracleSample(wl, 4, 2, microbatches)
+    s = OracleSample(wl, 4, 2, microbatches, hpz)
     t = time.perf_counter()
     s.run()
     dt = max(time.perf_counter() - t, 1e-4)
     scale = max(1.0, seconds / dt)
-    return OracleSample(wl, int(4 * scale), int(2 * scale), microbatches)
+    return OracleSample(wl, int(4 * scale), int(2 * scale), microbatches, hpz)
 
 
-def cpu_baseline(wl, seconds=12.0, microbatches=1):
-    s = sized_sample(wl, seconds / 2, microbatches)
+def cpu_baseline(wl, seconds=12.0, microbatches=1, hpz=False):
+    s = sized_sample(wl, seconds / 2, microbatches, hpz)
     t = time.perf_counter()
     n = 0
     while True:
@@ -556,7 +584,7 @@ def run_reference(args, wl):
     """The reference arm: the CPU oracle as it stands, on the host cores."""
     budget = 150.0
     per_step = max(0.2, min(5.0, budget / max(1, args.steps + args.warmup)))
-    s = sized_sample(wl, per_step, args.microbatches)
+    s = sized_sample(wl, per_step, args.microbatches, args.hpz)
     for _ in range(args.warmup):
         s.run()
     t = time.perf_counter()
@@ -569,7 +597,7 @@ def run_reference(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded counter-based generator, bounded sample of the workload",
-        "config": workload_config(wl, args.config, microbatches=args.microbatches),
+        "config": workload_config(wl, args.config, microbatches=args.microbatches, hpz=args.hpz),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{s.steps_bytes / 1e6:.1f} MB of algorithmic traffic per "
                                    "step: the first blocks of every shard and slice of every "
@@ -688,6 +716,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fuse-qwz", action="store_true",
                     help="produce the weights' qwZ message inside the final hop's Adam pass")
+    ap.add_argument("--hpz", action="store_true",
+                    help="add the hpZ backward weight gather from the secondary partitions")
     ap.add_argument("--microbatches", type=int, default=1,
                     help="gradient accumulation: micro-batches summed before the qgZ reduce")
     ap.add_argument("--no-cpu", action="store_true")
@@ -722,7 +752,7 @@ def main():
     try:
         res = run_gpu(args, wl, rank, world, device)
         if rank == 0 and world == 1 and not args.no_cpu:
-            res["cpu_baseline"] = cpu_baseline(wl, microbatches=args.microbatches)
+            res["cpu_baseline"] = cpu_baseline(wl, microbatches=args.microbatches, hpz=args.hpz)
         if rank == 0:
             print(json.dumps(res), flush=True)
     finally:

@@ -22,7 +22,8 @@ ZPP_OK, ZPP_ERR_INVALID_ARG, ZPP_ERR_MISALIGNED, ZPP_ERR_UNSUPPORTED, ZPP_ERR_CU
 # every symbol include/zpp.h declares
 EXPORTS = (
     "zpp_qwz_quant", "zpp_qwz_dequant", "zpp_qgz_reorder_quant", "zpp_grad_accumulate",
-    "zpp_qgz_reorder_quant_acc", "zpp_qgz_hop_reduce", "zpp_qgz_final_hop_adam_qwz", "zpp_shard_adam_step", "zpp_codes_bytes", "zpp_num_blocks", "zpp_qgz_slice_perm",
+    "zpp_qgz_reorder_quant_acc", "zpp_qgz_hop_reduce", "zpp_qgz_final_hop_adam_qwz",
+    "zpp_hpz_gather", "zpp_hpz_secondary_bytes", "zpp_shard_adam_step", "zpp_codes_bytes", "zpp_num_blocks", "zpp_qgz_slice_perm",
     "zpp_status_string", "zpp_last_cuda_error", "zpp_abi_version",
 )
 
@@ -73,6 +74,8 @@ def _lib():
         "zpp_qgz_hop_reduce": (I32, [I32, P, P, I32, I32, I64, I32, I32, P, P, P, HP, ST, P]),
         "zpp_qgz_final_hop_adam_qwz": (I32, [I32, P, P, I32, I32, I64, I32, I32, P, HP, ST, I32, P,
                                               P, P]),
+        "zpp_hpz_gather": (I32, [I32, I32, I64, I32, I32, P, P, P, P]),
+        "zpp_hpz_secondary_bytes": (I64, [I32, I64, I32, I32]),
         "zpp_shard_adam_step": (I32, [P, I64, HP, ST, P]),
         "zpp_codes_bytes": (I64, [I64, I32]),
         "zpp_num_blocks": (I64, [I64, I32]),
@@ -205,6 +208,31 @@ def zpp_qgz_final_hop_adam_qwz(hop, codes_in, scales_in, nodes, gpus_per_node, b
         gpus_per_node, bucket_elems, block, bits, _dev(grad_out, _F32, "grad_out"), hp, st,
         qwz_bits, _dev(qwz_codes, _BYTES, "qwz_codes"), _dev(qwz_scales, _F32, "qwz_scales"),
         _stream(stream, codes_in)), "zpp_qgz_final_hop_adam_qwz")
+
+
+def zpp_hpz_gather(gpus_per_node, shards_per_rank, shard_elems, block, bits, sec_codes,
+                   sec_scales, y_bf16, stream=None):
+    """`sec_codes`/`sec_scales`: one device tensor (or pointer) per local rank
+    (`sec_scales` None for bits 16)."""
+    G = len(sec_codes)
+    if G != gpus_per_node:
+        raise ValueError("one secondary partition per local rank")
+    cp = (ctypes.c_void_p * G)(*[_dev(t, _BF16 if bits == 16 else _BYTES, "sec_codes")
+                                 for t in sec_codes])
+    sp = None
+    if bits != 16:
+        if sec_scales is None or len(sec_scales) != G:
+            raise ValueError("one scale tensor per local rank")
+        sp = (ctypes.c_void_p * G)(*[_dev(t, _F32, "sec_scales") for t in sec_scales])
+    _check(_lib().zpp_hpz_gather(gpus_per_node, shards_per_rank, shard_elems, block, bits,
+                                 ctypes.cast(cp, ctypes.c_void_p),
+                                 None if sp is None else ctypes.cast(sp, ctypes.c_void_p),
+                                 _dev(y_bf16, _BF16, "y_bf16"), _stream(stream, y_bf16)),
+           "zpp_hpz_gather")
+
+
+def zpp_hpz_secondary_bytes(shards_per_rank, shard_elems, block, bits):
+    return int(_lib().zpp_hpz_secondary_bytes(shards_per_rank, shard_elems, block, bits))
 
 
 def zpp_shard_adam_step(grad, n, adam, state, stream=None):

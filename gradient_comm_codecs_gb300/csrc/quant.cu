@@ -293,83 +293,117 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantArgs a) {
   }
 }
 
+// Rows (shards) come from up to kMaxSources separate buffers: source s holds
+// rows s*rows_per_src .. s*rows_per_src + rows_per_src - 1, back to back
+// (row_code_bytes of codes and row_blocks scales each).  The qwZ receiver is
+// the one-source case; the hpZ backward gather reads the G secondary
+// partitions of a node.
+constexpr int kMaxSources = kMaxHpzSources;
+
 struct DequantArgs {
-  const uint8_t* codes;
-  const float* scales;
+  const uint8_t* codes[kMaxSources];
+  const float* scales[kMaxSources];
   uint16_t* y;
   int64_t total_units, units_per_row;
-  int64_t row_len, row_blocks;
+  int64_t row_len, row_blocks, row_code_bytes, rows_per_src;
 };
 
-// y = bf16_rn((float)q * s) for every element of every shard.
+template <int BITS>
+struct RowWord {  // the 8-element load of one lane: codes, or bf16 values when BITS == 16
+  using T = typename CodeVec<BITS>::T;
+};
+template <>
+struct RowWord<16> {
+  using T = uint4;
+};
+
+// y = bf16_rn((float)q * s) for every element of every row; BITS == 16
+// copies bf16 rows unchanged.
 template <int BITS, int LOGB>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) {
-  using G = Geo<LOGB, kQRows>;
   constexpr int K = kQRows;
-  constexpr int WE = G::kWarpElems;
-  using CW = typename CodeVec<BITS>::T;
+  constexpr int WE = 256 * K;
+  using CW = typename RowWord<BITS>::T;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t u, uend;
   unit_range(a.total_units, (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps, u, uend);
   if (u >= uend) return;
   int64_t row = u / a.units_per_row;
   int64_t t = u - row * a.units_per_row;
+  const uint8_t* crow;
+  const float* srow;
+  uint16_t* yrow;
+  bool row_aligned;
+  auto set_row = [&]() {
+    const int64_t s = row / a.rows_per_src, j = row - s * a.rows_per_src;
+    crow = a.codes[s] + j * a.row_code_bytes;
+    srow = BITS == 16 ? nullptr : a.scales[s] + j * a.row_blocks;
+    yrow = a.y + row * a.row_len;
+    row_aligned = ((reinterpret_cast<uintptr_t>(crow) % sizeof(CW)) |
+                   (reinterpret_cast<uintptr_t>(yrow) & 15)) == 0;
+  };
+  set_row();
   for (; u < uend; ++u) {
-    const int64_t base = row * a.row_len;
     const int64_t e_warp = t * WE;
     const int64_t valid = a.row_len - e_warp;
-    const bool full = ((base & 7) == 0) && valid >= WE;
-    const uint8_t* cw = a.codes + (((base + e_warp) * BITS) >> 3);
-    const float* sw = a.scales + row * a.row_blocks;
-    uint16_t* yw = a.y + base + e_warp;
-    if (full) {
+    const uint8_t* cw = crow + ((e_warp * BITS) >> 3);
+    uint16_t* yw = yrow + e_warp;
+    if (row_aligned && valid >= WE) {
       CW w[K];
       float s[K];
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int e = k * 256 + lane * 8;
         w[k] = __ldcs(reinterpret_cast<const CW*>(cw + ((e * BITS) >> 3)));
-        s[k] = __ldg(sw + ((e_warp + e) >> LOGB));
+        if constexpr (BITS != 16) s[k] = __ldg(srow + ((e_warp + e) >> LOGB));
       }
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int e = k * 256 + lane * 8;
-        float q[8];
-        decode8<BITS>(w[k], q);
-        const float2 s2 = make_float2(s[k], s[k]);
+        if constexpr (BITS == 16) {
+          __stcs(reinterpret_cast<uint4*>(yw + e), w[k]);
+        } else {
+          float q[8];
+          decode8<BITS>(w[k], q);
+          const float2 s2 = make_float2(s[k], s[k]);
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const float2 v = mul2(make_float2(q[i], q[i + 1]), s2);
-          q[i] = v.x;
-          q[i + 1] = v.y;
+          for (int i = 0; i < 8; i += 2) {
+            const float2 v = mul2(make_float2(q[i], q[i + 1]), s2);
+            q[i] = v.x;
+            q[i + 1] = v.y;
+          }
+          __stcs(reinterpret_cast<uint4*>(yw + e),
+                 make_uint4(pack_bf16x2(q[0], q[1]), pack_bf16x2(q[2], q[3]),
+                            pack_bf16x2(q[4], q[5]), pack_bf16x2(q[6], q[7])));
         }
-        __stcs(reinterpret_cast<uint4*>(yw + e),
-               make_uint4(pack_bf16x2(q[0], q[1]), pack_bf16x2(q[2], q[3]),
-                          pack_bf16x2(q[4], q[5]), pack_bf16x2(q[6], q[7])));
       }
     } else {
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int e = k * 256 + lane * 8;
         for (int i = 0; i < 8; ++i) {
-          const int64_t el = e_warp + e + i;
+          const int64_t el = e_warp + e + i;  // element within the row
           if (el >= a.row_len) break;
-          const int64_t pos = base + el;
-          int q;
-          if constexpr (BITS == 8) {
-            q = (int8_t)a.codes[pos];
+          if constexpr (BITS == 16) {
+            yw[e + i] = reinterpret_cast<const uint16_t*>(crow)[el];
           } else {
-            const uint8_t b = a.codes[pos >> 1];
-            const int nib = (pos & 1) ? (b >> 4) : (b & 0xF);
-            q = nib >= 8 ? nib - 16 : nib;
+            int q;
+            if constexpr (BITS == 8) {
+              q = (int8_t)crow[el];
+            } else {
+              const uint8_t b = crow[el >> 1];
+              const int nib = (el & 1) ? (b >> 4) : (b & 0xF);
+              q = nib >= 8 ? nib - 16 : nib;
+            }
+            yw[e + i] = bf16_bits(__fmul_rn((float)q, srow[el >> LOGB]));
           }
-          yw[e + i] = bf16_bits(__fmul_rn((float)q, sw[el >> LOGB]));
         }
       }
     }
     if (++t == a.units_per_row) {
       t = 0;
       ++row;
+      if (u + 1 < uend) set_row();
     }
   }
 }
@@ -401,13 +435,20 @@ cudaError_t run_quant(const QuantArgs& a0, int block, cudaStream_t st) {
 
 template <int BITS>
 cudaError_t run_dequant(const DequantArgs& a0, int block, cudaStream_t st) {
-  return dispatch_logb(block, [&](auto lb) -> cudaError_t {
-    constexpr int LOGB = decltype(lb)::value;
-    const void* k = reinterpret_cast<const void*>(&dequant_kernel<BITS, LOGB>);
-    dequant_kernel<BITS, LOGB>
+  if constexpr (BITS == 16) {  // a copy: the block size plays no part
+    const void* k = reinterpret_cast<const void*>(&dequant_kernel<16, 12>);
+    dequant_kernel<16, 12>
         <<<grid_for(k, (a0.total_units + kWarps - 1) / kWarps), kThreads, 0, st>>>(a0);
     return cudaGetLastError();
-  });
+  } else {
+    return dispatch_logb(block, [&](auto lb) -> cudaError_t {
+      constexpr int LOGB = decltype(lb)::value;
+      const void* k = reinterpret_cast<const void*>(&dequant_kernel<BITS, LOGB>);
+      dequant_kernel<BITS, LOGB>
+          <<<grid_for(k, (a0.total_units + kWarps - 1) / kWarps), kThreads, 0, st>>>(a0);
+      return cudaGetLastError();
+    });
+  }
 }
 
 // acc = (first ? 0 : acc) + (float)g for n elements; 8 per lane per step
@@ -476,18 +517,42 @@ cudaError_t launch_qgz_reorder_quant(const uint16_t* x, const float* acc, int32_
   return bits == 8 ? run_quant<8, true, false>(a, block, st) : run_quant<4, true, false>(a, block, st);
 }
 
+namespace {
+cudaError_t run_gather(DequantArgs& a, int64_t rows, int64_t shard, int32_t block, int32_t bits,
+                       cudaStream_t st) {
+  a.units_per_row = (shard + 256 * kQRows - 1) / (256 * kQRows);
+  a.total_units = rows * a.units_per_row;
+  a.row_len = shard;
+  a.row_blocks = (shard + block - 1) / block;
+  a.row_code_bytes = shard * bits / 8;
+  if (bits == 16) return run_dequant<16>(a, block, st);
+  return bits == 8 ? run_dequant<8>(a, block, st) : run_dequant<4>(a, block, st);
+}
+}  // namespace
+
 cudaError_t launch_qwz_dequant(const void* codes, const float* scales, int64_t nranks,
                                int64_t shard, int32_t block, int32_t bits, uint16_t* y,
                                cudaStream_t st) {
   DequantArgs a{};
-  a.codes = static_cast<const uint8_t*>(codes);
-  a.scales = scales;
+  a.codes[0] = static_cast<const uint8_t*>(codes);
+  a.scales[0] = scales;
   a.y = y;
-  a.units_per_row = (shard + 1023) / 1024;
-  a.total_units = nranks * a.units_per_row;
-  a.row_len = shard;
-  a.row_blocks = (shard + block - 1) / block;
-  return bits == 8 ? run_dequant<8>(a, block, st) : run_dequant<4>(a, block, st);
+  a.rows_per_src = nranks;
+  return run_gather(a, nranks, shard, block, bits, st);
+}
+
+cudaError_t launch_hpz_gather(int32_t G, int32_t N, int64_t shard, int32_t block, int32_t bits,
+                              const void* const* sec_codes, const float* const* sec_scales,
+                              uint16_t* y, cudaStream_t st) {
+  if (G > kMaxSources) return cudaErrorInvalidValue;
+  DequantArgs a{};
+  for (int l = 0; l < G; ++l) {
+    a.codes[l] = static_cast<const uint8_t*>(sec_codes[l]);
+    a.scales[l] = bits == 16 ? nullptr : sec_scales[l];
+  }
+  a.y = y;
+  a.rows_per_src = N;
+  return run_gather(a, (int64_t)G * N, shard, block, bits, st);
 }
 
 }  // namespace zpp

@@ -181,6 +181,38 @@ zpp_status zpp_qgz_reorder_quant(const uint16_t* grads_bf16, int32_t nodes,
                                               static_cast<cudaStream_t>(stream)));
 }
 
+zpp_status zpp_hpz_gather(int32_t gpus_per_node, int32_t shards_per_rank, int64_t shard_elems,
+                          int32_t block, int32_t bits, const void* const* sec_codes,
+                          const float* const* sec_scales, uint16_t* y_bf16, void* stream) {
+  if (gpus_per_node < 1 || gpus_per_node > kMaxHpzSources || shards_per_rank < 1 ||
+      shard_elems < 0 || !valid_block(block) || !(bits == 16 || valid_bits(bits)))
+    return ZPP_ERR_INVALID_ARG;
+  if (bits == 4 && (shard_elems & 1)) return ZPP_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)gpus_per_node * shards_per_rank;
+  if (shard_elems > 0 && rows > kMaxElems / shard_elems) return ZPP_ERR_INVALID_ARG;
+  if (shard_elems == 0) return ZPP_OK;
+  if (!sec_codes || !y_bf16 || (bits != 16 && !sec_scales)) return ZPP_ERR_INVALID_ARG;
+  for (int l = 0; l < gpus_per_node; ++l) {
+    if (!sec_codes[l] || (bits != 16 && !sec_scales[l])) return ZPP_ERR_INVALID_ARG;
+    if (!aligned16(sec_codes[l]) || (bits != 16 && !aligned16(sec_scales[l])))
+      return ZPP_ERR_MISALIGNED;
+  }
+  if (!aligned16(y_bf16)) return ZPP_ERR_MISALIGNED;
+  return cuda_status(launch_hpz_gather(gpus_per_node, shards_per_rank, shard_elems, block, bits,
+                                       sec_codes, sec_scales, y_bf16,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int64_t zpp_hpz_secondary_bytes(int32_t shards_per_rank, int64_t shard_elems, int32_t block,
+                                int32_t bits) {
+  if (shards_per_rank < 1 || shard_elems < 0 || !valid_block(block)) return -1;
+  if (shard_elems > kMaxElems / shards_per_rank) return -1;
+  if (bits == 16) return (int64_t)shards_per_rank * 2 * shard_elems;
+  if (!valid_bits(bits)) return -1;
+  return (int64_t)shards_per_rank *
+         (zpp_codes_bytes(shard_elems, bits) + 4 * zpp_num_blocks(shard_elems, block));
+}
+
 zpp_status zpp_grad_accumulate(const uint16_t* grads_bf16, float* acc, int64_t n, int32_t first,
                                void* stream) {
   if (n < 0 || n > kMaxElems || (first != 0 && first != 1)) return ZPP_ERR_INVALID_ARG;

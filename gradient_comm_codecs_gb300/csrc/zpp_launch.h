@@ -20,6 +20,11 @@ struct AdamConstsHost {
 //          position p = (j % G) * N + j / G.
 cudaError_t launch_qwz_quant(const uint16_t* x, int64_t nranks, int64_t shard, int32_t block,
                              int32_t bits, void* codes, float* scales, cudaStream_t st);
+// hpZ backward gather: G sources of N rows (shards) each; bits 16 copies bf16.
+constexpr int kMaxHpzSources = 64;
+cudaError_t launch_hpz_gather(int32_t G, int32_t N, int64_t shard, int32_t block, int32_t bits,
+                              const void* const* sec_codes, const float* const* sec_scales,
+                              uint16_t* y, cudaStream_t st);
 // acc: null, or the fp32 accumulator of earlier micro-batches (quantizes acc + x).
 cudaError_t launch_qgz_reorder_quant(const uint16_t* x, const float* acc, int32_t N, int32_t G,
                                      int64_t bucket, int32_t block, int32_t bits, void* codes,

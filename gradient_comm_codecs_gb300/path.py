@@ -6,6 +6,10 @@ the C-ABI calls in order.  One pass (``CodecPath.run``) is
   qwZ   zpp_qwz_quant (every rank's weight shard) -> zpp_qwz_dequant (the
         all-gather receiver, one full bf16 copy), optionally over several
         chunks of a long weight tensor;
+  hpZ   optionally the backward all-gather from the node's secondary
+        partitions (zpp_hpz_gather): local rank l keeps the received messages
+        of shards l*N .. l*N + N - 1, and the backward pass re-gathers the
+        weights from those G buffers into the same workspace;
   qgZ   zpp_qgz_reorder_quant (every rank's bucket) -> zpp_qgz_hop_reduce(1)
         -> zpp_qgz_hop_reduce(2) when there is more than one node, the final
         hop applying the Adam step to every rank's owned slice.  With M > 1
@@ -35,6 +39,7 @@ class QwzSpec:
     bits: int = 8
     chunks: int = 1          # the weight tensor is `chunks` calls of nranks*shard
     tail_shard: int = 0      # shard of the last call when nonzero
+    nodes: int = 1           # hpZ: the nranks ranks are `nodes` nodes of nranks/nodes GPUs
 
     def call_shards(self):
         s = [self.shard] * self.chunks
@@ -91,8 +96,12 @@ class CodecPath:
 
     def __init__(self, qwz: QwzSpec | None, qgz: QgzSpec | None, adam: AdamSpec | None,
                  device="cuda", keep_grad: bool = False, write_param: bool = True,
-                 fuse_qwz: bool = False, microbatches: int = 1, standalone_adam: int = 0):
-        """standalone_adam: parameters of a separate owned shard stepped by
+                 fuse_qwz: bool = False, microbatches: int = 1, standalone_adam: int = 0,
+                 hpz: bool = False):
+        """hpz: after the forward gather, the backward gather of the weights
+        from the secondary partitions (qwZ with one call, nranks divisible by
+        the node count).
+        standalone_adam: parameters of a separate owned shard stepped by
         zpp_shard_adam_step after the reduce (fp32 ``sa_grad``, ``sa_master``,
         ``sa_m``, ``sa_v``, bf16 ``sa_param``).
         microbatches: gradients of that many micro-batches (``grads_mb``,
@@ -112,6 +121,9 @@ class CodecPath:
                   and qwz.block == qgz.block)
             if not ok:
                 raise ValueError("fuse_qwz needs qwZ shards equal to the owned qgZ slices")
+        self.hpz = hpz
+        if hpz and (qwz is None or qwz.chunks != 1 or qwz.nranks % qwz.nodes):
+            raise ValueError("hpz needs one qwZ call over nodes x GPUs-per-node shards")
         self.device = torch.device(device)
         dev = self.device
         self.launches_per_run = 0
@@ -124,7 +136,7 @@ class CodecPath:
             self.w_scales = [_empty(qwz.nranks * Z.zpp_num_blocks(s, qwz.block), torch.float32, dev)
                              for s in sorted(set(shards))]
             self.w_full = _empty(qwz.phi, torch.bfloat16, dev)
-            self.launches_per_run += (1 if fuse_qwz else 2) * len(shards)
+            self.launches_per_run += (1 if fuse_qwz else 2) * len(shards) + (1 if hpz else 0)
         if qgz is not None:
             nd, b = qgz.nd, qgz.bucket
             self.grads_mb = [_empty(nd * b, torch.bfloat16, dev) for _ in range(microbatches)]
@@ -188,6 +200,24 @@ class CodecPath:
             if mark:
                 mark("qwz_dequant")
             off += n
+
+    def secondary_partitions(self):
+        """(codes, scales) views of every local rank's secondary partition:
+        the received messages of its N shards, kept from the forward gather."""
+        q = self.qwz
+        N, G = q.nodes, q.nranks // q.nodes
+        cb, nb = Z.zpp_codes_bytes(q.shard, q.bits), Z.zpp_num_blocks(q.shard, q.block)
+        c, s = self.w_codes[0], self.w_scales[0]
+        return ([c[l * N * cb:(l + 1) * N * cb] for l in range(G)],
+                [s[l * N * nb:(l + 1) * N * nb] for l in range(G)])
+
+    def run_hpz(self, stream=None, mark=None):
+        q = self.qwz
+        codes, scales = self.secondary_partitions()
+        Z.zpp_hpz_gather(q.nranks // q.nodes, q.nodes, q.shard, q.block, q.bits, codes, scales,
+                         self.w_full, stream)
+        if mark:
+            mark("hpz_gather")
 
     def run_qgz(self, stream=None, adam_step: int | None = None, mark=None):
         g = self.qgz
@@ -257,6 +287,8 @@ class CodecPath:
     def run(self, stream=None, adam_step: int | None = None, mark=None):
         if self.qwz is not None:
             self.run_qwz(stream, mark)
+        if self.hpz:
+            self.run_hpz(stream, mark)
         if self.qgz is not None:
             self.run_qgz(stream, adam_step, mark)
         if self.standalone_adam:

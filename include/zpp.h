@@ -216,6 +216,40 @@ zpp_status zpp_qgz_final_hop_adam_qwz(int32_t hop, const void* codes_in, const f
                                       const zpp_adam_state* state, int32_t qwz_bits,
                                       void* qwz_codes, float* qwz_scales, void* stream);
 
+/* ---- hpZ ------------------------------------------------------------------ */
+
+/* zpp_hpz_gather -- the backward weight all-gather of one node under hpZ,
+ * read from the node's secondary partitions.
+ * ("Quantized LLM Training at Scale with ZeRO++", 2 HPZ: every node keeps a
+ * secondary replica of the model partitions, so the backward all-gather
+ * reads only the node's own GPUs and moves nothing across nodes.)
+ *   gpus_per_node    G, 1..64: one secondary partition per local rank.
+ *   shards_per_rank  N (the number of nodes): local rank l's secondary
+ *                    partition is slice l of the G-way split of the weights,
+ *                    the N primary shards l*N .. l*N + N - 1, kept in the form
+ *                    the forward all-gather delivered them.
+ *   shard_elems      elements of one primary shard (even for bits 4).
+ *   bits 8 or 4      sec_codes[l] [N][zpp_codes_bytes(shard, bits)] and
+ *                    sec_scales[l] [N][zpp_num_blocks(shard, block)] (device,
+ *                    read): the qwZ messages of those shards.
+ *   bits 16          sec_codes[l] [N][shard] bf16 values; sec_scales unused
+ *                    (may be NULL); block must still be valid.
+ *   sec_codes, sec_scales: host arrays of G device pointers.
+ *   y_bf16           [G*N][shard] bf16 (device, written): the full weights;
+ *                    shard d = l*N + j is the j-th shard of sec_codes[l],
+ *                    dequantized exactly as zpp_qwz_dequant does.
+ * Errors: ZPP_ERR_INVALID_ARG (G outside 1..64, N < 1, sizes, bits, block,
+ * NULL pointers), ZPP_ERR_MISALIGNED (a pointer not 16-byte aligned). */
+zpp_status zpp_hpz_gather(int32_t gpus_per_node, int32_t shards_per_rank, int64_t shard_elems,
+                          int32_t block, int32_t bits, const void* const* sec_codes,
+                          const float* const* sec_scales, uint16_t* y_bf16, void* stream);
+
+/* Bytes of one rank's secondary partition under hpZ: N shards of codes and
+ * scales (bits 4/8) or of bf16 values (bits 16); -1 on bad args.  The G ranks
+ * of a node together hold one full replica of the weights. */
+int64_t zpp_hpz_secondary_bytes(int32_t shards_per_rank, int64_t shard_elems, int32_t block,
+                                int32_t bits);
+
 /* ---- sharded mixed-precision Adam ------------------------------------------ */
 
 /* zpp_shard_adam_step -- one Adam step on n owned parameters.

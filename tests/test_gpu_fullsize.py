@@ -277,3 +277,26 @@ def test_sweep_points(index):
     check_qgz(path, wl, nsample=1)
     del path
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("nodes", [1, 2, 4])
+def test_llama_hpz_backward_gather_full_size(nodes):
+    """The llama-layer weights on nodes x (8 / nodes) ranks: the backward
+    gather from the secondary partitions rebuilds exactly the weights of the
+    forward all-gather."""
+    Z = zpp()
+    wl = W.WORKLOADS["llama"]
+    q = wl.qwz
+    qs = Z.QwzSpec(q.nranks, q.shard, q.block, q.bits, nodes=nodes)
+    torch.cuda.empty_cache()
+    path = Z.CodecPath(qs, None, None, device="cuda", hpz=True)
+    synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, qs.phi, out=path.w)
+    path.run_qwz()
+    fwd = path.w_full.clone()
+    path.w_full.zero_()
+    path.run_hpz()
+    torch.cuda.synchronize()
+    assert torch.equal(path.w_full.view(torch.int16), fwd.view(torch.int16))
+    check_qwz(path, wl)
+    del path, fwd
+    torch.cuda.empty_cache()

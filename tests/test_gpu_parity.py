@@ -531,3 +531,68 @@ def test_sixteen_byte_aligned_state(bits, N, G):
         Z.zpp_grad_accumulate(synth.u16_to_bf16(mb).cuda(), acc, n, k == 0)
     torch.cuda.synchronize()
     assert_f32_bitexact(np_f32(acc), oracle.grad_accumulate(mbs), "accumulator")
+
+
+# ---- next row: hpZ node-local backward gather from secondary partitions -------------------------
+
+def _hpz_case(N, G, shard, block, bits, rng):
+    """Forward qwZ messages of N_d shards and the G secondary partitions kept
+    from them, each a separate device allocation."""
+    Nd = N * G
+    w = oracle.f32_to_bf16((rng.standard_normal(Nd * shard) * 0.02).astype(np.float32))
+    if bits == 16:
+        secs = [w[l * N * shard:(l + 1) * N * shard].copy() for l in range(G)]
+        dev = [synth.u16_to_bf16(s).cuda() for s in secs]
+        return w, secs, dev, None
+    c, s = oracle.qwz_quant(w, Nd, shard, block, bits)
+    cb, nb = oracle.codes_bytes(shard, bits), oracle.num_blocks(shard, block)
+    secs = [(c[l * N * cb:(l + 1) * N * cb].copy(), s[l * N * nb:(l + 1) * N * nb].copy())
+            for l in range(G)]
+    return (c, s), secs, [torch.from_numpy(a).cuda() for a, _ in secs], \
+        [torch.from_numpy(b).cuda() for _, b in secs]
+
+
+@pytest.mark.parametrize("bits", [16, 8, 4])
+@pytest.mark.parametrize("shard,block", [(4096, 256), (3 * 1024 + 64, 64), (2 * 4096, 2048),
+                                         (1000, 128), (514, 512), (2, 64)])
+@pytest.mark.parametrize("N,G", [(1, 8), (2, 4), (4, 2), (3, 3), (2, 8), (1, 1)])
+def test_hpz_gather(bits, shard, block, N, G):
+    Z = zpp()
+    fwd, secs, dc, ds = _hpz_case(N, G, shard, block, bits, RNG)
+    want = oracle.hpz_gather(secs, N, shard, block, bits)
+    y = torch.full((N * G * shard,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    Z.zpp_hpz_gather(G, N, shard, block, bits, dc, ds, y)
+    torch.cuda.synchronize()
+    assert_bytes_equal(u16(y), want, "hpZ backward gather")
+    if bits != 16:   # the same weights the forward all-gather delivered
+        c, s = fwd
+        yf = torch.empty_like(y)
+        Z.zpp_qwz_dequant(torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda(), N * G, shard,
+                          block, bits, yf)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), yf.view(torch.int16))
+
+
+def test_hpz_arguments():
+    import ctypes
+    Z = zpp()
+    c = [torch.zeros(4096, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    s = [torch.zeros(64, device="cuda") for _ in range(2)]
+    y = torch.zeros(2 * 4096, dtype=torch.bfloat16, device="cuda")
+    Z.zpp_hpz_gather(2, 1, 4096, 64, 8, c, s, y)
+    lib = Z._lib._lib()
+    cp = (ctypes.c_void_p * 65)(*([c[0].data_ptr()] * 65))
+    sp = (ctypes.c_void_p * 65)(*([s[0].data_ptr()] * 65))
+    P = lambda a: ctypes.cast(a, ctypes.c_void_p)   # noqa: E731
+    for args in ((65, 1, 4096, 64, 8), (0, 1, 4096, 64, 8), (2, 0, 4096, 64, 8),
+                 (2, 1, 4096, 48, 8), (2, 1, 4095, 64, 4), (2, 1, 4096, 64, 2)):
+        assert lib.zpp_hpz_gather(*args, P(cp), P(sp), y.data_ptr(), None) == \
+            Z.ZPP_ERR_INVALID_ARG, args
+    assert lib.zpp_hpz_gather(2, 1, 4096, 64, 8, P(cp), None, y.data_ptr(), None) == \
+        Z.ZPP_ERR_INVALID_ARG
+    with pytest.raises(Z.ZppError) as e:
+        Z.zpp_hpz_gather(2, 1, 4096, 64, 8, [c[0], c[1][4:]], s, y)
+    assert e.value.status == Z.ZPP_ERR_MISALIGNED
+    assert Z.zpp_hpz_secondary_bytes(2, 4096, 256, 8) == oracle.hpz_secondary_bytes(2, 4096, 256, 8)
+    assert Z.zpp_hpz_secondary_bytes(2, 4096, 256, 16) == 2 * 2 * 4096
+    assert Z.zpp_hpz_secondary_bytes(0, 4096, 256, 8) == -1
