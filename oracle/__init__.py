@@ -77,6 +77,8 @@ def _load():
         "orc_qgz_reorder_quant_f32": (I32, [P, I32, I32, I64, I64, I32, P, P]),
         "orc_hpz_gather": (I32, [I32, I32, I64, I64, I32, P, P, P]),
         "orc_hpz_secondary_bytes": (I64, [I32, I64, I64, I32]),
+        "orc_ring_rs_step": (I32, [I32, I32, I64, I64, I32, P, P, P, P, P, P]),
+        "orc_ring_reduce_scatter": (I32, [I32, I64, I64, I32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -348,3 +350,40 @@ def hpz_gather(secondaries, N: int, shard: int, block: int, bits: int) -> np.nda
 
 def hpz_secondary_bytes(N: int, shard: int, block: int, bits: int) -> int:
     return int(_load().orc_hpz_secondary_bytes(N, shard, block, bits))
+
+
+def ring_rs_step(step: int, nd: int, bucket: int, block: int, bits: int, grads_bf16,
+                 codes_in=None, scales_in=None):
+    """One step of the quantized ring reduce-scatter (the comparator of qgZ's
+    one-shot quantization).  Returns (codes, scales), or the fp32 gradient
+    [N_d][L] at the last step."""
+    x = _c(grads_bf16, np.uint16)
+    assert x.size == nd * bucket
+    L = bucket // nd
+    if step == nd - 1:
+        g = np.zeros(nd * L, dtype=np.float32)
+        _check(_load().orc_ring_rs_step(step, nd, bucket, block, bits, _ptr(x),
+                                        _ptr(None if codes_in is None else np.ascontiguousarray(codes_in)),
+                                        _ptr(None if scales_in is None else _c(scales_in, np.float32)),
+                                        None, None, _ptr(g)), "ring_rs_step")
+        return g
+    if bits == 32:
+        codes = np.zeros(nd * L, dtype=np.float32)
+    else:
+        codes = np.zeros(nd * codes_bytes(L, bits), dtype=np.uint8)
+    scales = np.zeros(nd * num_blocks(L, block), dtype=np.float32)
+    ci = None if codes_in is None else np.ascontiguousarray(codes_in)
+    si = None if scales_in is None else _c(scales_in, np.float32)
+    _check(_load().orc_ring_rs_step(step, nd, bucket, block, bits, _ptr(x), _ptr(ci), _ptr(si),
+                                    _ptr(codes), _ptr(scales), None), "ring_rs_step")
+    return codes, scales
+
+
+def ring_reduce_scatter(grads_bf16, nd: int, bucket: int, block: int, bits: int) -> np.ndarray:
+    """The whole quantized ring: rank r's averaged chunk r, [N_d][L] fp32."""
+    x = _c(grads_bf16, np.uint16)
+    assert x.size == nd * bucket
+    g = np.zeros(bucket, dtype=np.float32)
+    _check(_load().orc_ring_reduce_scatter(nd, bucket, block, bits, _ptr(x), _ptr(g)),
+           "ring_reduce_scatter")
+    return g

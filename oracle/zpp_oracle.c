@@ -484,3 +484,87 @@ int64_t orc_hpz_secondary_bytes(int N, int64_t shard, int64_t block, int bits)
     if (bits != 8 && bits != 4) return -1;
     return (int64_t)N * (orc_codes_bytes(shard, bits) + 4 * orc_num_blocks(shard, block));
 }
+
+/* ---- ring reduce-scatter with a requantization at every hop (comparator) --
+ * [P1] section 3 (QGZ), challenge "sequential quantization overhead": in a
+ * ring reduce-scatter of quantized gradients every GPU on the ring
+ * dequantizes, adds and requantizes, N sequential quantizations where qgZ
+ * does one.  This is the comparator for that precision loss.
+ * Reading: ring r -> r + 1 (mod N_d); chunk c = elements [c*L, (c+1)*L) of a
+ * rank's bucket, L = bucket / N_d; at step s = 0..N_d-1 rank r works on chunk
+ * c = (r - 1 - s) mod N_d:
+ *   s = 0            msg_r = Q(x_r[c])
+ *   0 < s < N_d - 1  msg_r = Q(D(msg_{r-1}) + x_r[c])
+ *   s = N_d - 1      g_r   = (D(msg_{r-1}) + x_r[c]) * (1.0f / N_d),  c = r
+ * so chunk c is summed in the ring order c+1, c+2, ..., c and rank r ends with
+ * the average of its own chunk, as the reduce-scatter of qgZ delivers it.
+ * Q is the block quantization (blocks restart at the chunk start), D its
+ * dequantization, + one rounded fp32 add.  With N_d == 1 the only step is the
+ * last one and g = x. */
+
+static int64_t ring_chunk(int r, int s, int nd)
+{
+    return (((int64_t)r - 1 - s) % nd + nd) % nd;
+}
+
+int orc_ring_rs_step(int step, int nd, int64_t bucket, int64_t block, int bits,
+                     const uint16_t* x, const void* codes_in, const float* scales_in,
+                     void* codes_out, float* scales_out, float* grad_out)
+{
+    if (nd <= 0 || step < 0 || step >= nd || bucket < 0 || block <= 0 || !valid_bits(bits))
+        return ORC_EINVAL;
+    if (bucket % ((int64_t)nd * block)) return ORC_EINVAL;
+    const int64_t L = bucket / nd;
+    const int64_t cb = orc_codes_bytes(L, bits), nb = orc_num_blocks(L, block);
+    float* v = (float*)malloc((size_t)(L > 0 ? L : 1) * sizeof(float));
+    if (!v) return ORC_EINVAL;
+    const int last = (step == nd - 1);
+    for (int r = 0; r < nd; ++r) {
+        const int64_t c = ring_chunk(r, step, nd);
+        const uint16_t* xr = x + (int64_t)r * bucket + c * L;
+        const int prev = (r - 1 + nd) % nd;
+        for (int64_t i = 0; i < L; ++i) {
+            float own = bf16_to_f32(xr[i]);
+            if (step == 0) {
+                v[i] = own;
+            } else {
+                float d = deq((const uint8_t*)codes_in + prev * cb, scales_in + prev * nb, i,
+                              block, bits);
+                v[i] = d + own;
+            }
+        }
+        if (last) {
+            const float inv = 1.0f / (float)nd;
+            for (int64_t i = 0; i < L; ++i) grad_out[(int64_t)r * L + i] = v[i] * inv;
+        } else {
+            orc_block_quant(v, L, block, bits, (uint8_t*)codes_out + r * cb, scales_out + r * nb);
+        }
+    }
+    free(v);
+    return ORC_OK;
+}
+
+/* The whole ring: N_d steps, messages passed between two buffers. */
+int orc_ring_reduce_scatter(int nd, int64_t bucket, int64_t block, int bits,
+                            const uint16_t* x, float* grad_out)
+{
+    if (nd <= 0 || bucket < 0 || block <= 0 || !valid_bits(bits)) return ORC_EINVAL;
+    if (bucket % ((int64_t)nd * block)) return ORC_EINVAL;
+    const int64_t L = bucket / nd;
+    const int64_t cb = orc_codes_bytes(L, bits), nb = orc_num_blocks(L, block);
+    uint8_t* c[2];
+    float* s[2];
+    for (int k = 0; k < 2; ++k) {
+        c[k] = (uint8_t*)calloc((size_t)(nd * cb > 0 ? nd * cb : 1), 1);
+        s[k] = (float*)calloc((size_t)(nd * nb > 0 ? nd * nb : 1), sizeof(float));
+    }
+    int rc = ORC_OK;
+    for (int step = 0; step < nd && rc == ORC_OK; ++step)
+        rc = orc_ring_rs_step(step, nd, bucket, block, bits, x, c[(step + 1) & 1],
+                              s[(step + 1) & 1], c[step & 1], s[step & 1], grad_out);
+    for (int k = 0; k < 2; ++k) {
+        free(c[k]);
+        free(s[k]);
+    }
+    return rc;
+}

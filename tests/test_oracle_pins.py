@@ -586,3 +586,99 @@ def test_hpz_secondary_memory_is_a_node_replica():
             assert oracle.hpz_secondary_bytes(N, shard, block, 16) == 2 * phi // G
     gv = golden("zeropp_volume.txt")
     assert Fraction(gv["hpz_bwd_cross_node_M"]) == 0
+
+
+# ---- next row: ring reduce-scatter with a requantization per hop (precision comparator) ----------
+
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 8])
+def test_ring_with_identity_codec_is_the_average(nd):
+    """Small integers sum exactly in fp32, so with the identity codec rank r
+    ends with sum_k x_k[chunk r] * fl(1/N_d), whatever the ring order."""
+    L, block = 3 * 64, 64
+    bucket = nd * L
+    xi = RNG.integers(-50, 51, size=(nd, nd, L))
+    x = oracle.f32_to_bf16(xi.astype(np.float32).reshape(-1))
+    g = oracle.ring_reduce_scatter(x, nd, bucket, block, 32)
+    want = xi.sum(axis=0).astype(np.float32) * np.float32(1.0 / nd)
+    assert np.array_equal(g.reshape(nd, L), want)
+
+
+def test_ring_two_ranks_composed_from_block_codec():
+    """N_d = 2: chunk 0 goes 1 -> 0, so g_0 = (D(Q(x_1[0])) + x_0[0]) * 0.5 and
+    g_1 = (D(Q(x_0[1])) + x_1[1]) * 0.5."""
+    L, block = 4 * 64, 64
+    x = oracle.f32_to_bf16((RNG.standard_normal(2 * 2 * L) * 1e-3).astype(np.float32))
+    xf = oracle.bf16_bits_to_f32(x).reshape(2, 2, L)
+    for bits in (8, 4):
+        g = oracle.ring_reduce_scatter(x, 2, 2 * L, block, bits).reshape(2, L)
+        for r in (0, 1):
+            c, s = oracle.block_quant(xf[1 - r, r], block, bits)
+            d = oracle.block_dequant(c, s, L, block, bits)
+            want = (d + xf[r, r]) * np.float32(0.5)
+            assert np.array_equal(g[r], want.astype(np.float32))
+
+
+@pytest.mark.parametrize("nd", [3, 8])
+def test_ring_error_within_the_sum_of_half_scales(nd):
+    """Chunk c passes N_d - 1 quantizations on its way round the ring; each
+    moves an element by at most half its block's scale, so the result is
+    within (sum of those half scales) / N_d of the exact average (plus fp32
+    rounding of the adds)."""
+    L, block, bits = 2 * 128, 128, 4
+    bucket = nd * L
+    x = oracle.f32_to_bf16((RNG.standard_normal(nd * bucket) * 1e-3).astype(np.float32))
+    xf = oracle.bf16_bits_to_f32(x).reshape(nd, nd, L).astype(np.float64)
+    nb = L // block
+    half = np.zeros((nd, nb))          # per chunk, per block: sum of s/2 along the ring
+    ci = si = None
+    for step in range(nd):
+        out = oracle.ring_rs_step(step, nd, bucket, block, bits, x, ci, si)
+        if step == nd - 1:
+            g = out.reshape(nd, L)
+            break
+        ci, si = out
+        for r in range(nd):
+            c = (r - 1 - step) % nd
+            half[c] += si.reshape(nd, nb)[r] / 2
+    exact = xf.sum(axis=0) / nd
+    bound = np.repeat(half, block, axis=1) / nd + 1e-6 * np.abs(xf).sum(axis=0).max()
+    assert np.all(np.abs(g - exact) <= bound)
+    assert np.any(np.abs(g - exact) > 0.1 * bound)   # the bound is not vacuous
+
+
+def test_ring_error_grows_with_nd_and_exceeds_qgz():
+    """The pages' point: N sequential requantizations lose precision that the
+    one-shot quantization of qgZ does not.  On seeded N(0, 1e-3) gradients the
+    ring's relative RMS error grows with N_d while qgZ's stays flat."""
+    rng = np.random.default_rng(3)
+    block, bits = 256, 4
+    ring, qgz = [], []
+    for nd in (2, 4, 8, 16, 32):
+        L = 4 * block
+        bucket = nd * L
+        x = oracle.f32_to_bf16((rng.standard_normal(nd * bucket) * 1e-3).astype(np.float32))
+        xf = oracle.bf16_bits_to_f32(x).reshape(nd, nd, L).astype(np.float64)
+        exact = (xf.sum(axis=0) / nd).reshape(-1)
+        rms = np.sqrt(np.mean(exact ** 2))
+        N, G = (1, nd) if nd <= 8 else (nd // 8, 8)
+        gr = oracle.ring_reduce_scatter(x, nd, bucket, block, bits)
+        gq = oracle.qgz_reduce_scatter(x, N, G, bucket, block, bits)
+        ring.append(np.sqrt(np.mean((gr - exact) ** 2)) / rms)
+        qgz.append(np.sqrt(np.mean((gq - exact) ** 2)) / rms)
+    assert all(b > a for a, b in zip(ring, ring[1:]))
+    assert max(qgz) < 1.6 * min(qgz)
+    assert ring[2] > 1.5 * qgz[2] and ring[4] > 2.5 * qgz[4]
+
+
+def test_ring_sums_in_ring_order():
+    """N_d = 4, identity codec: chunk 0 is summed by ranks 1, 2, 3, then 0.
+    With x_1 = 2^24, x_2 = x_3 = 1, x_0 = -2^24 that order loses both ones
+    ((2^24 + 1) rounds to 2^24) and gives 0; the reverse ring direction
+    (3, 2, 1, 0) would give 2 / 4."""
+    nd, L, block = 4, 64, 64
+    xf = np.zeros((nd, nd, L), np.float32)
+    xf[1, 0], xf[2, 0], xf[3, 0], xf[0, 0] = 2.0 ** 24, 1.0, 1.0, -(2.0 ** 24)
+    x = oracle.f32_to_bf16(xf.reshape(-1))
+    g = oracle.ring_reduce_scatter(x, nd, nd * L, block, 32).reshape(nd, L)
+    assert np.all(g[0] == 0.0)
+    assert np.all(g[1:] == 0.0)
