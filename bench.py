@@ -50,12 +50,15 @@ KERNEL_OF = {  # launch name -> CUDA kernel (for the roofline and the ncu summar
     "grad_accumulate": "accumulate_kernel",
     "shard_adam": "adam_kernel<WIDE>",
     "hpz_gather": "dequant_kernel<BITS, LOGB> (G secondary sources)",
+    "ring_step": "ring_kernel<BITS, LOGB, MODE>",
+    "ring_adam": "adam_kernel<WIDE>",
     "qgz_reorder_quant_acc": "quant_tiled_kernel<BITS, true, LOGB, true>",
 }
 KERNEL_SRC = {"qwz_quant": "quant.cu", "qwz_dequant": "quant.cu", "qgz_reorder_quant": "quant.cu",
               "qgz_hop1": "hop.cu", "qgz_final_hop": "hop.cu", "qgz_final_hop_qwz": "hop.cu",
               "grad_accumulate": "quant.cu", "qgz_reorder_quant_acc": "quant.cu",
-              "shard_adam": "adam.cu", "hpz_gather": "quant.cu"}
+              "shard_adam": "adam.cu", "hpz_gather": "quant.cu", "ring_step": "ring.cu",
+              "ring_adam": "adam.cu"}
 
 
 # ---- workload -> algorithmic bytes ------------------------------------------------
@@ -68,7 +71,23 @@ def msg_bytes(n, block, bits):
     return codes_bytes(n, bits) + 4 * (-(-n // block))
 
 
-def launch_bytes(wl, fuse_qwz=False, microbatches=1, hpz=False):
+def ring_launch_bytes(g, fused_adam):
+    """[(launch, bytes)] of the quantized ring over qgZ workload `g`: at every
+    step each rank reads its bf16 chunk, the incoming message after the first
+    step, and writes the outgoing message (or the fp32 chunk at the last);
+    then the Adam step on the reduced gradient (30 B a parameter)."""
+    nd, L = g.nd, g.slice_elems
+    m = msg_bytes(L, g.block, g.bits)
+    out = []
+    for step in range(nd):
+        b = 2 * L + (m if step > 0 else 0) + (m if step < nd - 1 else 4 * L)
+        out.append(("ring_step", nd * b))
+    if fused_adam:
+        out.append(("ring_adam", 30 * g.bucket))
+    return out
+
+
+def launch_bytes(wl, fuse_qwz=False, microbatches=1, hpz=False, ring=False):
     """[(launch name, algorithmic bytes)] of one pass, in launch order.  With
     fuse_qwz the weights' qwZ message is written by the final hop's Adam pass
     (the next step's message), so the pass has no separate quantize launch.
@@ -93,7 +112,9 @@ def launch_bytes(wl, fuse_qwz=False, microbatches=1, hpz=False):
     if q is not None and hpz:
         out.append(("hpz_gather", q.nranks * msg_bytes(q.shard, q.block, q.bits)
                     + 2 * q.nranks * q.shard))
-    if g is not None:
+    if g is not None and ring:
+        out += ring_launch_bytes(g, wl.fused_adam)
+    elif g is not None:
         nd, b = g.nd, g.bucket
         m1 = nd * msg_bytes(b, g.block, g.bits)
         if microbatches > 1:
@@ -118,9 +139,12 @@ def launch_bytes(wl, fuse_qwz=False, microbatches=1, hpz=False):
     return out
 
 
-def workload_config(wl, name, fuse_qwz=False, microbatches=1, hpz=False):
+def workload_config(wl, name, fuse_qwz=False, microbatches=1, hpz=False, ring=False):
     q, g = wl.qwz, wl.qgz
     cfg = {"workload": wl.name, "name": name}
+    if ring:
+        cfg["reduce_scatter"] = ("comparator: quantized ring (a requantization at every hop, "
+                                 "N_d launches) + Adam on the reduced gradient, instead of qgZ")
     if hpz:
         cfg["hpz"] = ("backward weight gather from the node's secondary partitions "
                       f"({hpz_nodes(wl)} node(s) x {q.nranks // hpz_nodes(wl)} GPUs)")
@@ -139,7 +163,7 @@ def workload_config(wl, name, fuse_qwz=False, microbatches=1, hpz=False):
                    else "none")
     if wl.standalone_adam:
         cfg["standalone_adam_params"] = wl.standalone_adam
-    per_step = sum(b for _, b in launch_bytes(wl, fuse_qwz, microbatches, hpz))
+    per_step = sum(b for _, b in launch_bytes(wl, fuse_qwz, microbatches, hpz, ring))
     if per_step > 4 * L2_BYTES:
         cfg["l2"] = (f"inputs larger than L2: {per_step / 1e9:.2f} GB moved per step vs "
                      f"{L2_BYTES / 2**20:.0f} MiB L2; no flush")
@@ -312,12 +336,12 @@ def run_gpu(args, wl, rank, world, device):
     path = Z.CodecPath(qs, gs, adam, device=device, keep_grad=False, fuse_qwz=args.fuse_qwz,
                        microbatches=args.microbatches,
                        standalone_adam=wl.standalone_adam if adam is not None else 0,
-                       hpz=args.hpz)
+                       hpz=args.hpz, ring=args.ring)
     fill_inputs(path, wl)
     stream = torch.cuda.current_stream(device)
     if args.fuse_qwz:
         path.prime_fused_qwz(stream)
-    lb = launch_bytes(wl, args.fuse_qwz, args.microbatches, args.hpz)
+    lb = launch_bytes(wl, args.fuse_qwz, args.microbatches, args.hpz, args.ring)
     step_bytes = sum(b for _, b in lb)
 
     def one_step(i, events=None):
@@ -386,7 +410,7 @@ def run_gpu(args, wl, rank, world, device):
     dom = max(kernels, key=lambda k: kernels[k]["share"])
     traffic = traffic_table().get((dom, args.config + ("+fuse_qwz" if args.fuse_qwz else "")
                                    + (f"+mb{args.microbatches}" if args.microbatches > 1 else "")
-                                   + ("+hpz" if args.hpz else "")))
+                                   + ("+hpz" if args.hpz else "") + ("+ring" if args.ring else "")))
     dk = kernels[dom]
     roofline = {"bound": "hbm", "kernel": dk["kernel"], "launch": dom,
                 "achieved": dk["gbs"], "peak": peak, "unit": "GB/s",
@@ -395,7 +419,8 @@ def run_gpu(args, wl, rank, world, device):
                 "traffic": traffic, "algorithmic_bytes": dk["bytes_per_launch"]}
 
     value = whole_job_gbs(step_bytes, world, ms_step)
-    qgz_ms = sum(sum(per[n]) for n in per if n.startswith("qgz")) / args.steps
+    qgz_ms = sum(sum(per[n]) for n in per if n.startswith("qgz") or n.startswith("ring")) \
+        / args.steps
     qgz_eps = (g.nd * g.bucket / (qgz_ms * 1e-3)) if g else None
 
     # ---- end to end through the public API with host buffers ----
@@ -409,7 +434,8 @@ def run_gpu(args, wl, rank, world, device):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic: seeded counter-based generator (lowbias32 hash -> "
         "2^20-entry quantile table), weights N(0,0.02), grads per the workload",
-        "config": workload_config(wl, args.config, args.fuse_qwz, args.microbatches, args.hpz),
+        "config": workload_config(wl, args.config, args.fuse_qwz, args.microbatches, args.hpz,
+                                  args.ring),
         "pct_hbm_peak_measured": 100.0 * value / world / peak,
         "pct_hbm_peak_nominal": 100.0 * value / world / NOMINAL_HBM_GBS,
         "qgz_bucket_elems_per_s": qgz_eps * world if qgz_eps else None,
@@ -462,7 +488,7 @@ class OracleSample:
     blocks of every slice of every rank's bucket -- a self-contained smaller
     instance of the same pass (same topology, block, bits, Adam, micro-batches)."""
 
-    def __init__(self, wl, nbw, nbg, microbatches=1, hpz=False):
+    def __init__(self, wl, nbw, nbg, microbatches=1, hpz=False, ring=False):
         import numpy as np
         import synth
         from synth import workloads as W
@@ -492,22 +518,28 @@ class OracleSample:
             self.gx = self.mbs[-1]
             bucket = nd * Lm
             self.g = (g.nodes, g.gpus_per_node, bucket, g.block, g.bits)
+            self.ring = ring
             gidx = (np.arange(nd)[:, None] * g.slice_elems + np.arange(Lm)[None, :]).reshape(-1)
             import oracle
             self.master = oracle.bf16_bits_to_f32(synth.bf16_to_u16(
                 synth.at(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, gidx)))
             self.zero = np.zeros(bucket, np.float32)
             m1 = nd * msg_bytes(bucket, g.block, g.bits)
-            b = m1 + 2 * nd * bucket
-            if microbatches > 1:
-                b += 4 * nd * bucket + sum(6 if k == 0 else 10 for k in range(microbatches - 1)) \
-                    * nd * bucket
-            if g.nodes == 1:
-                b += m1
+            if ring:   # the same accounting as the GPU ring, on the sample's bucket
+                import dataclasses
+                gm = dataclasses.replace(g, bucket=bucket)
+                b = sum(x for _, x in ring_launch_bytes(gm, wl.fused_adam))
             else:
-                m2 = nd * msg_bytes(g.nodes * Lm, g.block, g.bits)
-                b += m1 + m2 + m2
-            b += (26 if wl.fused_adam else 4) * bucket
+                b = m1 + 2 * nd * bucket
+                if microbatches > 1:
+                    b += 4 * nd * bucket + sum(6 if k == 0 else 10
+                                               for k in range(microbatches - 1)) * nd * bucket
+                if g.nodes == 1:
+                    b += m1
+                else:
+                    m2 = nd * msg_bytes(g.nodes * Lm, g.block, g.bits)
+                    b += m1 + m2 + m2
+                b += (26 if wl.fused_adam else 4) * bucket
             self.steps_bytes += b
             self.elems = nd * bucket
         self.sa = None
@@ -534,7 +566,10 @@ class OracleSample:
                 oracle.hpz_gather([(c[l * N * cb:(l + 1) * N * cb], s[l * N * nb:(l + 1) * N * nb])
                                    for l in range(G)], N, n, block, bits)
         if self.g is not None:
-            if len(self.mbs) > 1:
+            if self.ring:
+                N, G, bucket, block, bits = self.g
+                gr = oracle.ring_reduce_scatter(self.gx, N * G, bucket, block, bits)
+            elif len(self.mbs) > 1:
                 N = self.g[0]
                 c1, s1 = oracle.qgz_reorder_quant_f32(oracle.grad_accumulate(self.mbs), *self.g)
                 if N == 1:
@@ -553,18 +588,18 @@ class OracleSample:
             oracle.adam_step(g, p, z, z, a.lr, a.beta1, a.beta2, a.eps, a.step)
 
 
-def sized_sample(wl, seconds, microbatches=1, hpz=False):
+def sized_sample(wl, seconds, microbatches=1, hpz=False, ring=False):
     """Calibrate the sample so one oracle pass takes about `seconds`."""
-    s = OracleSample(wl, 4, 2, microbatches, hpz)
+    s = OracleSample(wl, 4, 2, microbatches, hpz, ring)
     t = time.perf_counter()
     s.run()
     dt = max(time.perf_counter() - t, 1e-4)
     scale = max(1.0, seconds / dt)
-    return OracleSample(wl, int(4 * scale), int(2 * scale), microbatches, hpz)
+    return OracleSample(wl, int(4 * scale), int(2 * scale), microbatches, hpz, ring)
 
 
-def cpu_baseline(wl, seconds=12.0, microbatches=1, hpz=False):
-    s = sized_sample(wl, seconds / 2, microbatches, hpz)
+def cpu_baseline(wl, seconds=12.0, microbatches=1, hpz=False, ring=False):
+    s = sized_sample(wl, seconds / 2, microbatches, hpz, ring)
     t = time.perf_counter()
     n = 0
     while True:
@@ -584,7 +619,7 @@ def run_reference(args, wl):
     """The reference arm: the CPU oracle as it stands, on the host cores."""
     budget = 150.0
     per_step = max(0.2, min(5.0, budget / max(1, args.steps + args.warmup)))
-    s = sized_sample(wl, per_step, args.microbatches, args.hpz)
+    s = sized_sample(wl, per_step, args.microbatches, args.hpz, args.ring)
     for _ in range(args.warmup):
         s.run()
     t = time.perf_counter()
@@ -597,13 +632,67 @@ def run_reference(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded counter-based generator, bounded sample of the workload",
-        "config": workload_config(wl, args.config, microbatches=args.microbatches, hpz=args.hpz),
+        "config": workload_config(wl, args.config, microbatches=args.microbatches, hpz=args.hpz,
+                                  ring=args.ring),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{s.steps_bytes / 1e6:.1f} MB of algorithmic traffic per "
                                    "step: the first blocks of every shard and slice of every "
                                    "rank, single-threaded C oracle"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+# ---- the ring comparator sweep (precision and time against qgZ) -------------------------------
+
+RING_SWEEP_ND = (2, 4, 8, 16, 32, 64, 128)
+
+
+def run_ring_sweep(args):
+    """For N_d = 2..128 ranks of a 2^22-element bucket (N(0, 1e-3) bf16
+    gradients, int4, block 256): the quantized ring and the qgZ chain (1 x N_d
+    up to 8 ranks, N_d/8 nodes x 8 beyond) on the same data, their errors
+    against the float64 average of the bf16 inputs (relative RMS, max over
+    the RMS of the average) and their CUDA-event times.  One JSON line per
+    N_d."""
+    import torch
+    import gradient_comm_codecs_gb300 as Z
+    from gradient_comm_codecs_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+    bucket_per_rank, block, bits = 1 << 22, 256, 4
+    for nd in RING_SWEEP_ND:
+        N, G = (1, nd) if nd <= 8 else (nd // 8, 8)
+        b = bucket_per_rank
+        torch.manual_seed(nd)
+        qgz = Z.CodecPath(None, Z.QgzSpec(N, G, b, block, bits), None, device=dev, keep_grad=True)
+        qgz.grads.normal_(0.0, 1e-3)
+        ring = Z.CodecPath(None, Z.QgzSpec(N, G, b, block, bits), None, device=dev,
+                           keep_grad=True, ring=True)
+        ring.grads = qgz.grads          # the same gradients
+        exact = qgz.grads.view(nd, nd, b // nd).double().sum(0).reshape(-1) / nd
+        rms = exact.pow(2).mean().sqrt().item()
+        rec = {"N_d": nd, "topology": f"{N}x{G}", "bucket_per_rank": b, "block": block,
+               "bits": bits}
+        for name, path in (("qgz", qgz), ("ring", ring)):
+            path.run_qgz(st)
+            torch.cuda.synchronize()
+            err = path.grad_out.double() - exact
+            rec[f"{name}_rel_rmse"] = err.pow(2).mean().sqrt().item() / rms
+            rec[f"{name}_max_over_rms"] = err.abs().max().item() / rms
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(10):
+                path.run_qgz(st)
+            e1.record(st)
+            torch.cuda.synchronize()
+            rec[f"{name}_ms"] = e0.elapsed_time(e1) / 10
+        rec["rmse_ratio_ring_over_qgz"] = rec["ring_rel_rmse"] / rec["qgz_rel_rmse"]
+        rec["time_ratio_ring_over_qgz"] = rec["ring_ms"] / rec["qgz_ms"]
+        print(json.dumps(rec), flush=True)
+        del qgz, ring, exact
+        torch.cuda.empty_cache()
 
 
 # ---- the sweep (small-message efficiency) -----------------------------------------------------
@@ -716,6 +805,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fuse-qwz", action="store_true",
                     help="produce the weights' qwZ message inside the final hop's Adam pass")
+    ap.add_argument("--ring", action="store_true",
+                    help="comparator: reduce the gradients with the quantized ring instead of qgZ")
+    ap.add_argument("--ring-sweep", action="store_true",
+                    help="ring vs qgZ error and time over N_d = 2..128 (GPU), one JSON line each")
     ap.add_argument("--hpz", action="store_true",
                     help="add the hpZ backward weight gather from the secondary partitions")
     ap.add_argument("--microbatches", type=int, default=1,
@@ -738,6 +831,9 @@ def main():
     if args.sweep:
         run_sweep(args)
         return
+    if args.ring_sweep:
+        run_ring_sweep(args)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, wl)), flush=True)
@@ -752,7 +848,8 @@ def main():
     try:
         res = run_gpu(args, wl, rank, world, device)
         if rank == 0 and world == 1 and not args.no_cpu:
-            res["cpu_baseline"] = cpu_baseline(wl, microbatches=args.microbatches, hpz=args.hpz)
+            res["cpu_baseline"] = cpu_baseline(wl, microbatches=args.microbatches, hpz=args.hpz,
+                                               ring=args.ring)
         if rank == 0:
             print(json.dumps(res), flush=True)
     finally:

@@ -11,6 +11,6 @@ from ._lib import (  # noqa: F401
     ZppError, library_path, zpp_abi_version, zpp_adam_hparams, zpp_adam_state, zpp_codes_bytes,
     zpp_grad_accumulate, zpp_hpz_gather, zpp_hpz_secondary_bytes, zpp_num_blocks, zpp_qgz_final_hop_adam_qwz, zpp_qgz_hop_reduce,
     zpp_qgz_reorder_quant, zpp_qgz_reorder_quant_acc, zpp_qgz_slice_perm, zpp_qwz_dequant,
-    zpp_qwz_quant, zpp_shard_adam_step, zpp_status_string,
+    zpp_qwz_quant, zpp_ring_rs_step, zpp_shard_adam_step, zpp_status_string,
 )
 from .path import AdamSpec, CodecPath, QgzSpec, QwzSpec  # noqa: F401

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzpp.so")
-SOURCES = ["zpp_abi.cu", "quant.cu", "hop.cu", "adam.cu"]
+SOURCES = ["zpp_abi.cu", "quant.cu", "hop.cu", "adam.cu", "ring.cu"]
 HEADERS = [os.path.join(CSRC, "zpp_device.cuh"), os.path.join(CSRC, "zpp_launch.h"),
            os.path.join(INCLUDE, "zpp.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -23,7 +23,7 @@ ZPP_OK, ZPP_ERR_INVALID_ARG, ZPP_ERR_MISALIGNED, ZPP_ERR_UNSUPPORTED, ZPP_ERR_CU
 EXPORTS = (
     "zpp_qwz_quant", "zpp_qwz_dequant", "zpp_qgz_reorder_quant", "zpp_grad_accumulate",
     "zpp_qgz_reorder_quant_acc", "zpp_qgz_hop_reduce", "zpp_qgz_final_hop_adam_qwz",
-    "zpp_hpz_gather", "zpp_hpz_secondary_bytes", "zpp_shard_adam_step", "zpp_codes_bytes", "zpp_num_blocks", "zpp_qgz_slice_perm",
+    "zpp_hpz_gather", "zpp_hpz_secondary_bytes", "zpp_ring_rs_step", "zpp_shard_adam_step", "zpp_codes_bytes", "zpp_num_blocks", "zpp_qgz_slice_perm",
     "zpp_status_string", "zpp_last_cuda_error", "zpp_abi_version",
 )
 
@@ -74,6 +74,7 @@ def _lib():
         "zpp_qgz_hop_reduce": (I32, [I32, P, P, I32, I32, I64, I32, I32, P, P, P, HP, ST, P]),
         "zpp_qgz_final_hop_adam_qwz": (I32, [I32, P, P, I32, I32, I64, I32, I32, P, HP, ST, I32, P,
                                               P, P]),
+        "zpp_ring_rs_step": (I32, [I32, I32, I64, I32, I32, P, P, P, P, P, P, P]),
         "zpp_hpz_gather": (I32, [I32, I32, I64, I32, I32, P, P, P, P]),
         "zpp_hpz_secondary_bytes": (I64, [I32, I64, I32, I32]),
         "zpp_shard_adam_step": (I32, [P, I64, HP, ST, P]),
@@ -208,6 +209,18 @@ def zpp_qgz_final_hop_adam_qwz(hop, codes_in, scales_in, nodes, gpus_per_node, b
         gpus_per_node, bucket_elems, block, bits, _dev(grad_out, _F32, "grad_out"), hp, st,
         qwz_bits, _dev(qwz_codes, _BYTES, "qwz_codes"), _dev(qwz_scales, _F32, "qwz_scales"),
         _stream(stream, codes_in)), "zpp_qgz_final_hop_adam_qwz")
+
+
+def zpp_ring_rs_step(step, nranks, bucket_elems, block, bits, grads_bf16, codes_in=None,
+                     scales_in=None, codes_out=None, scales_out=None, grad_out=None, stream=None):
+    _check(_lib().zpp_ring_rs_step(step, nranks, bucket_elems, block, bits,
+                                   _dev(grads_bf16, _BF16, "grads_bf16"),
+                                   _dev(codes_in, _BYTES, "codes_in"),
+                                   _dev(scales_in, _F32, "scales_in"),
+                                   _dev(codes_out, _BYTES, "codes_out"),
+                                   _dev(scales_out, _F32, "scales_out"),
+                                   _dev(grad_out, _F32, "grad_out"), _stream(stream, grads_bf16)),
+           "zpp_ring_rs_step")
 
 
 def zpp_hpz_gather(gpus_per_node, shards_per_rank, shard_elems, block, bits, sec_codes,

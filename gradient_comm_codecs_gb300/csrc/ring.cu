@@ -1,0 +1,153 @@
+// ring.cu -- one step of a ring reduce-scatter of quantized gradients, for
+// every simulated rank at once: the precision (and time) comparator of qgZ.
+//
+// ("Quantized LLM Training at Scale with ZeRO++", 3 QGZ, the challenge of
+// sequential quantization: in a ring reduce-scatter every GPU dequantizes the
+// partial sum it receives, adds its own gradient chunk and requantizes it for
+// the next GPU, N sequential quantizations where qgZ's one-shot scheme has one.)
+//
+// Ring r -> r + 1 (mod N_d); chunk c = elements [c*L, (c+1)*L) of a rank's
+// bucket; at step s rank r works on chunk c = (r - 1 - s) mod N_d:
+//   s = 0            msg_r = Q(x_r[c])
+//   0 < s < N_d - 1  msg_r = Q(D(msg_{r-1}) + x_r[c])
+//   s = N_d - 1      g_r   = (D(msg_{r-1}) + x_r[r]) * (1.0f / N_d)
+// Q is the block quantization of the other codecs (blocks restart at the chunk
+// start), D = (float)q * s, + one rounded fp32 add.
+//
+// Streaming, like the one-shot quantizer: 2 B of own gradient in, plus the
+// incoming message (bits/8 + 4/B B) after the first step, and the outgoing
+// message (or 4 B of fp32 gradient at the last step) out, per element.
+#include "zpp_device.cuh"
+#include "zpp_launch.h"
+
+namespace zpp {
+namespace {
+
+constexpr int kRingRows = 4;  // rows of 256 elements per warp slab
+
+struct RingArgs {
+  const uint16_t* x;          // [N_d][bucket] bf16
+  const uint8_t* codes_in;    // [N_d][cb]: the message each rank received
+  const float* scales_in;     // [N_d][nb]
+  uint8_t* codes_out;         // [N_d][cb]
+  float* scales_out;          // [N_d][nb]
+  float* grad_out;            // [N_d][L] (last step)
+  int64_t bucket, L, cb, nb;
+  int64_t units_per_row, total_units;
+  int32_t nd, step;
+  float inv_nd;
+};
+
+enum { kRingFirst = 0, kRingMiddle = 1, kRingLast = 2 };
+
+template <int BITS, int LOGB, int MODE>
+__global__ void __launch_bounds__(kThreads) ring_kernel(const RingArgs a) {
+  using G = Geo<LOGB, kRingRows>;
+  constexpr int K = kRingRows;
+  constexpr int GPC = kWarps / G::WPB;
+  using CW = typename CodeVec<BITS>::T;
+  __shared__ float red[2][kWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = warp / G::WPB, wsub = warp - gid * G::WPB;
+  int64_t u, uend;
+  unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
+  if (u >= uend) return;  // the whole group shares the range
+  int64_t r = u / a.units_per_row;
+  int64_t t = u - r * a.units_per_row;
+  const bool has_input = MODE == kRingMiddle || (MODE == kRingLast && a.step > 0);
+  int parity = 0;
+  for (; u < uend; ++u, parity ^= 1) {
+    const int64_t c = ((r - 1 - a.step) % a.nd + a.nd) % a.nd;
+    const int64_t prev = (r - 1 + a.nd) % a.nd;
+    const uint16_t* xrow = a.x + r * a.bucket + c * a.L;
+    const uint8_t* crow = a.codes_in + prev * a.cb;
+    const float* srow = a.scales_in + prev * a.nb;
+    const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;
+    const int64_t valid = a.L - e_warp;  // a multiple of 64 when positive
+    float v[K][8];
+    int nv[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int e = k * 256 + lane * 8;
+      nv[k] = (int64_t)e < valid ? 8 : 0;
+      if (nv[k]) {
+        unpack_bf16x8(__ldcs(reinterpret_cast<const uint4*>(xrow + e_warp + e)), v[k]);
+        if (has_input) {
+          float q[8];
+          decode8<BITS>(__ldcs(reinterpret_cast<const CW*>(crow + (((e_warp + e) * BITS) >> 3))), q);
+          const float s = __ldg(srow + ((e_warp + e) >> LOGB));
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[k][i] = __fadd_rn(__fmul_rn(q[i], s), v[k][i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[k][i] = 0.0f;
+      }
+    }
+    if constexpr (MODE == kRingLast) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        if (!nv[k]) continue;
+        float g[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g[i] = __fmul_rn(v[k][i], a.inv_nd);
+        st8_cs(a.grad_out + r * a.L + e_warp + k * 256 + lane * 8, false, g);
+      }
+    } else {
+      const int64_t dst = r * a.L;  // rank r's message starts at element r*L
+      quantize_unit<BITS, LOGB, G>(v, nv, true, dst, dst >> LOGB, e_warp, a.codes_out,
+                                   a.scales_out, red, parity, warp, gid, lane);
+    }
+    if (++t == a.units_per_row) {
+      t = 0;
+      ++r;
+    }
+  }
+}
+
+template <int BITS, int MODE>
+cudaError_t run_ring(RingArgs a, int block, cudaStream_t st) {
+  return dispatch_logb(block, [&](auto lb) -> cudaError_t {
+    constexpr int LOGB = decltype(lb)::value;
+    using G = Geo<LOGB, kRingRows>;
+    a.units_per_row = (a.L + G::U - 1) / G::U;
+    a.total_units = (int64_t)a.nd * a.units_per_row;
+    const int64_t groups = kWarps / G::WPB;
+    const void* k = reinterpret_cast<const void*>(&ring_kernel<BITS, LOGB, MODE>);
+    ring_kernel<BITS, LOGB, MODE>
+        <<<grid_for(k, (a.total_units + groups - 1) / groups), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+  });
+}
+
+template <int BITS>
+cudaError_t run_ring_mode(const RingArgs& a, int block, cudaStream_t st) {
+  if (a.step == a.nd - 1) return run_ring<BITS, kRingLast>(a, block, st);
+  if (a.step == 0) return run_ring<BITS, kRingFirst>(a, block, st);
+  return run_ring<BITS, kRingMiddle>(a, block, st);
+}
+
+}  // namespace
+
+cudaError_t launch_ring_rs_step(int32_t step, int32_t nd, int64_t bucket, int32_t block,
+                                int32_t bits, const uint16_t* x, const void* codes_in,
+                                const float* scales_in, void* codes_out, float* scales_out,
+                                float* grad_out, cudaStream_t st) {
+  RingArgs a{};
+  a.x = x;
+  a.codes_in = static_cast<const uint8_t*>(codes_in);
+  a.scales_in = scales_in;
+  a.codes_out = static_cast<uint8_t*>(codes_out);
+  a.scales_out = scales_out;
+  a.grad_out = grad_out;
+  a.bucket = bucket;
+  a.L = bucket / nd;
+  a.cb = a.L * bits / 8;
+  a.nb = a.L / block;
+  a.nd = nd;
+  a.step = step;
+  a.inv_nd = 1.0f / (float)nd;
+  return bits == 8 ? run_ring_mode<8>(a, block, st) : run_ring_mode<4>(a, block, st);
+}
+
+}  // namespace zpp

@@ -181,6 +181,27 @@ zpp_status zpp_qgz_reorder_quant(const uint16_t* grads_bf16, int32_t nodes,
                                               static_cast<cudaStream_t>(stream)));
 }
 
+zpp_status zpp_ring_rs_step(int32_t step, int32_t nranks, int64_t bucket_elems, int32_t block,
+                            int32_t bits, const uint16_t* grads_bf16, const void* codes_in,
+                            const float* scales_in, void* codes_out, float* scales_out,
+                            float* grad_out, void* stream) {
+  zpp_status s = check_topology(1, nranks, bucket_elems, block, bits);
+  if (s != ZPP_OK) return s;
+  if (step < 0 || step >= nranks) return ZPP_ERR_INVALID_ARG;
+  if (bucket_elems == 0) return ZPP_OK;
+  const bool first = step == 0, last = step == nranks - 1;
+  if (!grads_bf16 || (!first && (!codes_in || !scales_in)) ||
+      (!last && (!codes_out || !scales_out)) || (last && !grad_out))
+    return ZPP_ERR_INVALID_ARG;
+  if (!aligned16(grads_bf16) || (!first && (!aligned16(codes_in) || !aligned16(scales_in))) ||
+      (!last && (!aligned16(codes_out) || !aligned16(scales_out))) ||
+      (last && !aligned16(grad_out)))
+    return ZPP_ERR_MISALIGNED;
+  return cuda_status(launch_ring_rs_step(step, nranks, bucket_elems, block, bits, grads_bf16,
+                                         codes_in, scales_in, codes_out, scales_out, grad_out,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 zpp_status zpp_hpz_gather(int32_t gpus_per_node, int32_t shards_per_rank, int64_t shard_elems,
                           int32_t block, int32_t bits, const void* const* sec_codes,
                           const float* const* sec_scales, uint16_t* y_bf16, void* stream) {

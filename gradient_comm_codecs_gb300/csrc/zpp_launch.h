@@ -59,6 +59,12 @@ struct HopLaunch {
 };
 cudaError_t launch_hop_reduce(const HopLaunch& h, cudaStream_t st);
 
+// One step of the quantized ring reduce-scatter for all N_d ranks.
+cudaError_t launch_ring_rs_step(int32_t step, int32_t nd, int64_t bucket, int32_t block,
+                                int32_t bits, const uint16_t* x, const void* codes_in,
+                                const float* scales_in, void* codes_out, float* scales_out,
+                                float* grad_out, cudaStream_t st);
+
 cudaError_t launch_adam(const float* grad, int64_t n, const AdamConstsHost& ac, float* master,
                         float* m, float* v, uint16_t* param, cudaStream_t st);
 

@@ -18,6 +18,9 @@ the C-ABI calls in order.  One pass (``CodecPath.run``) is
         micro-batch (zpp_qgz_reorder_quant_acc).
   Adam  optionally zpp_shard_adam_step over a further owned shard (the part
         of a rank's parameters outside the reduced bucket).
+  ring  the comparator: the qgZ chain replaced by a ring reduce-scatter of
+        quantized gradients (N_d zpp_ring_rs_step launches, a requantization
+        at every hop) and zpp_shard_adam_step on the reduced gradient.
 
 Every message between two calls is a separate HBM buffer, as the wire
 between two GPUs would be.
@@ -97,8 +100,10 @@ class CodecPath:
     def __init__(self, qwz: QwzSpec | None, qgz: QgzSpec | None, adam: AdamSpec | None,
                  device="cuda", keep_grad: bool = False, write_param: bool = True,
                  fuse_qwz: bool = False, microbatches: int = 1, standalone_adam: int = 0,
-                 hpz: bool = False):
-        """hpz: after the forward gather, the backward gather of the weights
+                 hpz: bool = False, ring: bool = False):
+        """ring: reduce the gradients with the quantized ring instead of qgZ
+        (no micro-batches, no fused qwZ).
+        hpz: after the forward gather, the backward gather of the weights
         from the secondary partitions (qwZ with one call, nranks divisible by
         the node count).
         standalone_adam: parameters of a separate owned shard stepped by
@@ -122,6 +127,9 @@ class CodecPath:
             if not ok:
                 raise ValueError("fuse_qwz needs qwZ shards equal to the owned qgZ slices")
         self.hpz = hpz
+        self.ring = ring
+        if ring and (qgz is None or microbatches > 1 or fuse_qwz):
+            raise ValueError("ring replaces a plain qgZ chain")
         if hpz and (qwz is None or qwz.chunks != 1 or qwz.nranks % qwz.nodes):
             raise ValueError("hpz needs one qwZ call over nodes x GPUs-per-node shards")
         self.device = torch.device(device)
@@ -143,15 +151,23 @@ class CodecPath:
             self.grads = self.grads_mb[-1]
             self.acc = _empty(nd * b, torch.float32, dev) if microbatches > 1 else None
             self.launches_per_run += microbatches - 1
-            self.msg1 = _empty(nd * Z.zpp_codes_bytes(b, qgz.bits), torch.uint8, dev)
-            self.msg1_scales = _empty(nd * (b // qgz.block), torch.float32, dev)
-            self.launches_per_run += 2
-            if qgz.nodes > 1:
+            if ring:
+                L = qgz.L
+                self.ring_msgs = [(_empty(nd * Z.zpp_codes_bytes(L, qgz.bits), torch.uint8, dev),
+                                   _empty(nd * (L // qgz.block), torch.float32, dev))
+                                  for _ in range(2)]
+                self.launches_per_run += nd + (1 if adam is not None else 0)
+            else:
+                self.msg1 = _empty(nd * Z.zpp_codes_bytes(b, qgz.bits), torch.uint8, dev)
+                self.msg1_scales = _empty(nd * (b // qgz.block), torch.float32, dev)
+                self.launches_per_run += 2
+            if qgz.nodes > 1 and not ring:
                 nl = qgz.nodes * qgz.L
                 self.msg2 = _empty(nd * Z.zpp_codes_bytes(nl, qgz.bits), torch.uint8, dev)
                 self.msg2_scales = _empty(nd * (nl // qgz.block), torch.float32, dev)
                 self.launches_per_run += 1
-            self.grad_out = _empty(b, torch.float32, dev) if (keep_grad or adam is None) else None
+            self.grad_out = _empty(b, torch.float32, dev) \
+                if (keep_grad or adam is None or ring) else None
             if adam is not None:
                 self.master = _empty(b, torch.float32, dev)
                 self.m = torch.zeros(b, dtype=torch.float32, device=dev)
@@ -219,8 +235,29 @@ class CodecPath:
         if mark:
             mark("hpz_gather")
 
+    def run_ring(self, stream=None, adam_step: int | None = None, mark=None):
+        g = self.qgz
+        nd = g.nd
+        for step in range(nd):
+            ci, si = self.ring_msgs[(step + 1) & 1] if step else (None, None)
+            co, so = self.ring_msgs[step & 1] if step < nd - 1 else (None, None)
+            Z.zpp_ring_rs_step(step, nd, g.bucket, g.block, g.bits, self.grads, ci, si, co, so,
+                               self.grad_out if step == nd - 1 else None, stream)
+            if mark:
+                mark("ring_step")
+        if self.adam is not None:
+            hp = list(self.adam.hparams())
+            if adam_step is not None:
+                hp[4] = adam_step
+            Z.zpp_shard_adam_step(self.grad_out, g.bucket, tuple(hp),
+                                  (self.master, self.m, self.v, self.param), stream)
+            if mark:
+                mark("ring_adam")
+
     def run_qgz(self, stream=None, adam_step: int | None = None, mark=None):
         g = self.qgz
+        if self.ring:
+            return self.run_ring(stream, adam_step, mark)
         if self.microbatches > 1:
             n = g.nd * g.bucket
             for k, gk in enumerate(self.grads_mb[:-1]):

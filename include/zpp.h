@@ -216,6 +216,37 @@ zpp_status zpp_qgz_final_hop_adam_qwz(int32_t hop, const void* codes_in, const f
                                       const zpp_adam_state* state, int32_t qwz_bits,
                                       void* qwz_codes, float* qwz_scales, void* stream);
 
+/* zpp_ring_rs_step -- one step of a ring reduce-scatter of quantized
+ * gradients, for every rank at once: the comparator of the one-shot scheme.
+ * ("Quantized LLM Training at Scale with ZeRO++", 3 QGZ: a ring reduce-scatter
+ * of quantized gradients dequantizes and requantizes once per GPU on the
+ * ring -- N sequential quantizations, with their latency and precision loss
+ * -- where qgZ quantizes once.)
+ * Ring r -> r+1 (mod N_d); chunk c = elements [c*L, (c+1)*L) of a bucket,
+ * L = bucket_elems / N_d; at step s (0..N_d-1) rank r works on chunk
+ * c = (r - 1 - s) mod N_d:
+ *   s = 0            out_r = Q(x_r[c])
+ *   0 < s < N_d - 1  out_r = Q(D(in_{r-1}) + x_r[c])
+ *   s = N_d - 1      g_r   = (D(in_{r-1}) + x_r[r]) * (1.0f / N_d)
+ * Q: block quantization as zpp_qwz_quant (blocks restart at the chunk start),
+ * D: (float)q * s, +: one rounded fp32 add.  Chunk c is summed in the ring
+ * order c+1, c+2, ..., c; rank r ends with the average of chunk r, the
+ * element ownership of zpp_qgz_hop_reduce's final hop.
+ *   grads_bf16  [N_d][bucket_elems] bf16 (device, read).
+ *   codes_in    [N_d][zpp_codes_bytes(L, bits)], scales_in [N_d][L / block]:
+ *               the previous step's codes_out/scales_out (device, read;
+ *               unused, may be NULL, at step 0).
+ *   codes_out, scales_out: same shapes (device, written) for s < N_d - 1;
+ *               grad_out [N_d][L] fp32 (device, written) at s = N_d - 1.
+ * Requires bucket_elems % (N_d * block) == 0.  With N_d == 1 the only step is
+ * the last: g = x.
+ * Errors: ZPP_ERR_INVALID_ARG (step outside 0..N_d-1, sizes, missing
+ * buffers), ZPP_ERR_MISALIGNED. */
+zpp_status zpp_ring_rs_step(int32_t step, int32_t nranks, int64_t bucket_elems, int32_t block,
+                            int32_t bits, const uint16_t* grads_bf16, const void* codes_in,
+                            const float* scales_in, void* codes_out, float* scales_out,
+                            float* grad_out, void* stream);
+
 /* ---- hpZ ------------------------------------------------------------------ */
 
 /* zpp_hpz_gather -- the backward weight all-gather of one node under hpZ,

@@ -300,3 +300,38 @@ def test_llama_hpz_backward_gather_full_size(nodes):
     check_qwz(path, wl)
     del path, fwd
     torch.cuda.empty_cache()
+
+
+def test_two_hop_bucket_ring_reduce_scatter_full_size():
+    """The quantized ring over the two-hop workload's 16 ranks of 2^28-element
+    buckets, checked on sampled blocks of every chunk: blocks restart at chunk
+    starts, so the ring over those blocks alone reproduces them exactly."""
+    Z = zpp()
+    g = W.WORKLOADS["two_hop"].qgz
+    nd, bucket, B, bits = g.nd, g.bucket, g.block, g.bits
+    L = bucket // nd
+    torch.cuda.empty_cache()
+    x = grads_for(g, 0, device="cuda")
+    cb, nb = Z.zpp_codes_bytes(L, bits), L // B
+    bufs = [(torch.empty(nd * cb, dtype=torch.uint8, device="cuda"),
+             torch.empty(nd * nb, device="cuda")) for _ in range(2)]
+    grad = torch.full((bucket,), float("nan"), device="cuda")
+    for step in range(nd):
+        ci, si = bufs[(step + 1) & 1] if step else (None, None)
+        co, so = bufs[step & 1] if step < nd - 1 else (None, None)
+        Z.zpp_ring_rs_step(step, nd, bucket, B, bits, x, ci, si, co, so,
+                           grad if step == nd - 1 else None)
+    torch.cuda.synchronize()
+    blocks = sample_blocks(nb, 3, 11)
+    nbk = len(blocks)
+    # mini bucket: rank r, chunk c, sampled block q
+    pos = (np.arange(nd)[:, None, None] * L + np.asarray(blocks)[None, :, None] * B
+           + np.arange(B)[None, None, :]).reshape(-1)
+    mini = np.concatenate([synth.bf16_to_u16(synth.at(g.grad, 0, synth.grad_stream(r), pos))
+                           for r in range(nd)])
+    want = oracle.ring_reduce_scatter(mini, nd, nd * nbk * B, B, bits)
+    gidx = (np.arange(nd)[:, None, None] * L + np.asarray(blocks)[None, :, None] * B
+            + np.arange(B)[None, None, :]).reshape(-1)
+    assert_f32_bitexact(gather_f32(grad, gidx), want, "ring gradient")
+    del x, bufs, grad
+    torch.cuda.empty_cache()

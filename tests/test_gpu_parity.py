@@ -596,3 +596,74 @@ def test_hpz_arguments():
     assert Z.zpp_hpz_secondary_bytes(2, 4096, 256, 8) == oracle.hpz_secondary_bytes(2, 4096, 256, 8)
     assert Z.zpp_hpz_secondary_bytes(2, 4096, 256, 16) == 2 * 2 * 4096
     assert Z.zpp_hpz_secondary_bytes(0, 4096, 256, 8) == -1
+
+
+# ---- next row: quantized ring reduce-scatter (the comparator of qgZ's one-shot scheme) ----------
+
+def run_gpu_ring(Z, gb, nd, bucket, block, bits):
+    """Every step on the GPU; returns the messages of each step and the gradient."""
+    L = bucket // nd
+    x = synth.u16_to_bf16(gb).cuda()
+    cb, nb = Z.zpp_codes_bytes(L, bits), L // block
+    bufs = [(torch.full((nd * cb,), 0x5A, dtype=torch.uint8, device="cuda"),
+             torch.full((nd * nb,), float("nan"), device="cuda")) for _ in range(2)]
+    grad = torch.full((bucket,), float("nan"), device="cuda")
+    msgs = []
+    for step in range(nd):
+        ci, si = bufs[(step + 1) & 1] if step else (None, None)
+        co, so = bufs[step & 1] if step < nd - 1 else (None, None)
+        Z.zpp_ring_rs_step(step, nd, bucket, block, bits, x, ci, si, co, so,
+                           grad if step == nd - 1 else None)
+        if step < nd - 1:
+            torch.cuda.synchronize()
+            msgs.append((np_bytes(co).copy(), np_f32(so).copy()))
+    torch.cuda.synchronize()
+    return msgs, np_f32(grad)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("block,chunk_blocks", [(64, 3), (64, 16), (256, 5), (1024, 2),
+                                                (4096, 1)])
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 8, 16])
+def test_ring_reduce_scatter(bits, block, chunk_blocks, nd):
+    Z = zpp()
+    L = chunk_blocks * block
+    bucket = nd * L
+    if (nd + chunk_blocks) % 2:
+        x = special_values(nd * bucket, bits, block, RNG)
+    else:
+        x = (RNG.standard_t(3, nd * bucket) * 1e-3).astype(np.float32)
+    gb = oracle.f32_to_bf16(x)
+    msgs, g = run_gpu_ring(Z, gb, nd, bucket, block, bits)
+    ci = si = None
+    for step in range(nd - 1):
+        c, s = oracle.ring_rs_step(step, nd, bucket, block, bits, gb, ci, si)
+        assert_bytes_equal(msgs[step][0], c, f"ring step {step} codes")
+        assert_f32_bitexact(msgs[step][1], s, f"ring step {step} scales")
+        ci, si = c, s
+    want = oracle.ring_rs_step(nd - 1, nd, bucket, block, bits, gb, ci, si)
+    assert_f32_bitexact(g, want, "ring gradient")
+    assert_f32_bitexact(g, oracle.ring_reduce_scatter(gb, nd, bucket, block, bits),
+                        "ring gradient (whole ring)")
+
+
+def test_ring_arguments():
+    Z = zpp()
+    x = torch.zeros(4 * 256, dtype=torch.bfloat16, device="cuda")
+    c = torch.zeros(512, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(16, device="cuda")
+    g = torch.zeros(4 * 256, device="cuda")
+    Z.zpp_ring_rs_step(0, 2, 512, 64, 8, x, None, None, c, s)
+    for bad in ((2, 2), (-1, 2)):
+        with pytest.raises(Z.ZppError) as e:
+            Z.zpp_ring_rs_step(bad[0], bad[1], 512, 64, 8, x, c, s, c, s, g)
+        assert e.value.status == Z.ZPP_ERR_INVALID_ARG
+    with pytest.raises(Z.ZppError) as e:       # a middle step needs its input
+        Z.zpp_ring_rs_step(1, 4, 1024, 64, 8, x, None, None, c, s)
+    assert e.value.status == Z.ZPP_ERR_INVALID_ARG
+    with pytest.raises(Z.ZppError) as e:       # the last step writes the gradient
+        Z.zpp_ring_rs_step(1, 2, 512, 64, 8, x, c, s, None, None, None)
+    assert e.value.status == Z.ZPP_ERR_INVALID_ARG
+    with pytest.raises(Z.ZppError) as e:
+        Z.zpp_ring_rs_step(1, 2, 512, 64, 8, x, c, s, None, None, g[1:])
+    assert e.value.status == Z.ZPP_ERR_MISALIGNED
