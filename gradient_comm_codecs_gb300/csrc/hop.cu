@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
       for (int k = 0; k < K; ++k) {
         const int e = k * 256 + lane * 8;
         uint32_t c[8];
-        quantize8<QMAX>(acc[k], sc[k / RPB], c);  // every lane: it votes
+        quantize8<QMAX>(acc[k], sc[k / RPB], c);
         if (!on[k]) continue;
         *reinterpret_cast<CW*>(a.codes_out + (((obase + e) * BITS) >> 3)) = pack8<BITS>(c);
         if (((e_warp + e) & (G::B - 1)) == 0) a.scales_out[(obase + e) >> LOGB] = sc[k / RPB].s;

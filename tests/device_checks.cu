@@ -1,18 +1,23 @@
-// Exhaustive checks of device arithmetic identities the codec kernels rely on.
+// Checks of device arithmetic identities the codec kernels rely on.
 // Built and run by tests/test_gpu_device_identities.py on the GPU.
 //
 //  div_qmax<Q>(a) == __fdiv_rn(a, Q)   for every finite a >= 0, Q in {7, 127}
-//  |recip(s) - __frcp_rn(s)| <= 1 ulp  for every s in [2^-100, 2^126)
+//                                      (exhaustive: all 2^31 bit patterns)
+//  quantize8<Q>(x, make_scale<Q>(m)) == clamp(rint(__fdiv_rn(x, s)), -Q, Q)
+//      for seeded random block maxima m (s = fl(m / Q) in the fast range) and
+//      x drawn three ways: within 3 ulps of every (k + 1/2) s, |k| <= Q (the
+//      rounding boundaries), uniform in [-m, m], and those values truncated to
+//      bf16; 2^33 draws of 8 values each per divisor.
 #include <cstdio>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "zpp_device.cuh"
 
-__device__ unsigned long long g_bad[3];
-__device__ unsigned int g_first[3];
+__device__ unsigned long long g_bad[4];
+__device__ unsigned int g_first[4];
 
-__global__ void check(uint32_t lo, uint32_t hi) {
+__global__ void check_div(uint32_t lo, uint32_t hi) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t b = lo + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; b < hi; b += stride) {
     const float a = __uint_as_float((uint32_t)b);
@@ -22,28 +27,86 @@ __global__ void check(uint32_t lo, uint32_t hi) {
     if (zpp::div_qmax<127>(a) != __fdiv_rn(a, 127.0f)) {
       if (atomicAdd(&g_bad[1], 1ull) == 0) g_first[1] = (uint32_t)b;
     }
-    if (a >= zpp::kFastMinScale && a < zpp::kFastMaxScale) {
-      const int d = (int)__float_as_uint(zpp::recip(a)) - (int)__float_as_uint(__frcp_rn(a));
-      if (d > 1 || d < -1) {
-        if (atomicAdd(&g_bad[2], 1ull) == 0) g_first[2] = (uint32_t)b;
-      }
+  }
+}
+
+// lowbias32 (Chris Wellons' published integer hash)
+__device__ __forceinline__ uint32_t mix(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7feb352du;
+  x ^= x >> 15;
+  x *= 0x846ca68bu;
+  x ^= x >> 16;
+  return x;
+}
+
+template <int Q>
+__device__ void check_one(uint64_t t, int slot) {
+  uint32_t h = mix((uint32_t)t ^ mix((uint32_t)(t >> 32) + 0x9e3779b9u + slot));
+  // block maximum: log-uniform exponent over the fast scale range, random mantissa
+  const int ex = (int)(h % 216u) - 96;  // 2^-96 .. 2^119
+  h = mix(h);
+  float m = ldexpf(1.0f + (float)(h >> 9) * (1.0f / 8388608.0f), ex);
+  if (h & 1u) m = __uint_as_float(__float_as_uint(m) & 0xFFFF0000u);  // a bf16 maximum
+  const zpp::Scale sc = zpp::make_scale<Q>(m);
+  if (!sc.fast || sc.s == 0.0f) return;
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    h = mix(h + (uint32_t)i);
+    const uint32_t kind = h & 3u;
+    float v;
+    if (kind <= 1) {  // next to a rounding boundary (k + 1/2) s
+      const int k = (int)((h >> 2) % (uint32_t)(Q + 1)) - (int)((h >> 12) & 1u) * (Q + 1);
+      const int j = (int)((h >> 13) % 7u) - 3;
+      const float b = __fmul_rn((float)k + 0.5f, sc.s);
+      v = __int_as_float(__float_as_int(b) + j);
+    } else {  // uniform in [-m, m]
+      const float u = (float)(int)(h >> 8) * (1.0f / 8388608.0f) - 1.0f;
+      v = __fmul_rn(u, m);
+    }
+    if ((h >> 20) & 1u) v = __uint_as_float(__float_as_uint(v) & 0xFFFF0000u);  // bf16
+    if (!(fabsf(v) <= m)) v = 0.0f;  // a block never holds more than its maximum
+    x[i] = v;
+  }
+  uint32_t out[8];
+  zpp::quantize8<Q>(x, sc, out);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float r = rintf(__fdiv_rn(x[i], sc.s));
+    r = fminf(fmaxf(r, -(float)Q), (float)Q);
+    const int want = (int)r;
+    const int got = (int)out[i] - (int)zpp::kShiftBits;
+    const int c = Q == 7 ? 2 : 3;
+    if (got != want) {
+      if (atomicAdd(&g_bad[c], 1ull) == 0) g_first[c] = __float_as_uint(x[i]);
     }
   }
 }
 
+__global__ void check_quant(uint64_t n) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += stride) {
+    check_one<7>(t, 0);
+    check_one<127>(t, 1);
+  }
+}
+
 int main() {
-  unsigned long long zero[3] = {0, 0, 0};
+  unsigned long long zero[4] = {0, 0, 0, 0};
   if (cudaMemcpyToSymbol(g_bad, zero, sizeof zero) != cudaSuccess) return 2;
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
-  check<<<sms * 8, 256>>>(0u, 0x7F800000u);  // +0 .. largest finite
+  check_div<<<sms * 8, 256>>>(0u, 0x7F800000u);  // +0 .. largest finite
+  check_quant<<<sms * 8, 256>>>(1ull << 33);
   if (cudaDeviceSynchronize() != cudaSuccess) return 3;
-  unsigned long long bad[3];
-  unsigned int first[3];
+  unsigned long long bad[4];
+  unsigned int first[4];
   cudaMemcpyFromSymbol(bad, g_bad, sizeof bad);
   cudaMemcpyFromSymbol(first, g_first, sizeof first);
   printf("div_qmax7 %llu %08x\n", bad[0], bad[0] ? first[0] : 0u);
   printf("div_qmax127 %llu %08x\n", bad[1], bad[1] ? first[1] : 0u);
-  printf("recip_1ulp %llu %08x\n", bad[2], bad[2] ? first[2] : 0u);
+  printf("quantize_q7 %llu %08x\n", bad[2], bad[2] ? first[2] : 0u);
+  printf("quantize_q127 %llu %08x\n", bad[3], bad[3] ? first[3] : 0u);
   return 0;
 }
