@@ -41,6 +41,7 @@ struct HopArgs {
   uint8_t* qwz_codes;      // final hop + Adam + qwZ: next step's weight message
   float* qwz_scales;
   bool wide;               // grad_out, master, m, v (those given) 32-byte aligned
+  float one;               // 1.0f, read at run time (see accumulate8)
 };
 
 // kFinalAdamQwz: the final hop, the Adam step, and the int8 block
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
         for (int k = 0; k < K; ++k) {
           float q[8];
           decode8<BITS>(ch.c[j][k], q);
-          accumulate8(acc[k], q, ch.s[j][k / RPB]);
+          accumulate8(acc[k], q, ch.s[j][k / RPB], a.one);
         }
       }
     };
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
         for (int k = 0; k < K; ++k) {
           float q[8];
           decode8<BITS>(ch.c[j][k], q);
-          accumulate8(acc[k], q, ch.s[j][k / RPB]);
+          accumulate8(acc[k], q, ch.s[j][k / RPB], a.one);
         }
       }
     };
@@ -457,6 +458,7 @@ cudaError_t launch_hop_reduce(const HopLaunch& h, cudaStream_t st) {
   a.param = h.param;
   a.qwz_codes = static_cast<uint8_t*>(h.qwz_codes);
   a.qwz_scales = h.qwz_scales;
+  a.one = 1.0f;
   a.wide = (!a.grad_out || aligned32(a.grad_out)) &&
            (!h.adam || (aligned32(a.master) && aligned32(a.m) && aligned32(a.v)));
   const int b = h.block;

@@ -36,6 +36,7 @@ struct RingArgs {
   int64_t units_per_row, total_units;
   int32_t nd, step;
   float inv_nd;
+  float one;  // 1.0f, read at run time (see accumulate8)
 };
 
 enum { kRingFirst = 0, kRingMiddle = 1, kRingLast = 2 };
@@ -56,12 +57,40 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const RingArgs a) {
   int64_t t = u - r * a.units_per_row;
   const bool has_input = MODE == kRingMiddle || (MODE == kRingLast && a.step > 0);
   int parity = 0;
-  for (; u < uend; ++u, parity ^= 1) {
-    const int64_t c = ((r - 1 - a.step) % a.nd + a.nd) % a.nd;
-    const int64_t prev = (r - 1 + a.nd) % a.nd;
-    const uint16_t* xrow = a.x + r * a.bucket + c * a.L;
+  // The next unit's loads are issued before the current unit is computed.
+  struct Loads {
+    uint4 x[K];
+    CW c[K];
+    float s[K];
+  };
+  auto load = [&](Loads& l, int64_t rr, int64_t tt) {
+    const int64_t c = ((rr - 1 - a.step) % a.nd + a.nd) % a.nd;
+    const int64_t prev = (rr - 1 + a.nd) % a.nd;
+    const uint16_t* xrow = a.x + rr * a.bucket + c * a.L;
     const uint8_t* crow = a.codes_in + prev * a.cb;
     const float* srow = a.scales_in + prev * a.nb;
+    const int64_t ew = tt * G::U + (int64_t)wsub * G::kWarpElems;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int64_t e = ew + k * 256 + lane * 8;
+      if (e < a.L) {
+        l.x[k] = __ldcs(reinterpret_cast<const uint4*>(xrow + e));
+        if (has_input) {
+          l.c[k] = __ldcs(reinterpret_cast<const CW*>(crow + ((e * BITS) >> 3)));
+          l.s[k] = __ldg(srow + (e >> LOGB));
+        }
+      }
+    }
+  };
+  Loads cur, nxt;
+  load(cur, r, t);
+  for (; u < uend; ++u, parity ^= 1) {
+    int64_t rn = r, tn = t + 1;
+    if (tn == a.units_per_row) {
+      tn = 0;
+      ++rn;
+    }
+    if (u + 1 < uend) load(nxt, rn, tn);
     const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;
     const int64_t valid = a.L - e_warp;  // a multiple of 64 when positive
     float v[K][8];
@@ -71,13 +100,11 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const RingArgs a) {
       const int e = k * 256 + lane * 8;
       nv[k] = (int64_t)e < valid ? 8 : 0;
       if (nv[k]) {
-        unpack_bf16x8(__ldcs(reinterpret_cast<const uint4*>(xrow + e_warp + e)), v[k]);
+        unpack_bf16x8(cur.x[k], v[k]);
         if (has_input) {
           float q[8];
-          decode8<BITS>(__ldcs(reinterpret_cast<const CW*>(crow + (((e_warp + e) * BITS) >> 3))), q);
-          const float s = __ldg(srow + ((e_warp + e) >> LOGB));
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[k][i] = __fadd_rn(__fmul_rn(q[i], s), v[k][i]);
+          decode8<BITS>(cur.c[k], q);
+          accumulate8(v[k], q, cur.s[k], a.one);  // own + D(msg), each rounded
         }
       } else {
 #pragma unroll
@@ -98,10 +125,9 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const RingArgs a) {
       quantize_unit<BITS, LOGB, G>(v, nv, true, dst, dst >> LOGB, e_warp, a.codes_out,
                                    a.scales_out, red, parity, warp, gid, lane);
     }
-    if (++t == a.units_per_row) {
-      t = 0;
-      ++r;
-    }
+    r = rn;
+    t = tn;
+    cur = nxt;
   }
 }
 
@@ -147,6 +173,7 @@ cudaError_t launch_ring_rs_step(int32_t step, int32_t nd, int64_t bucket, int32_
   a.nd = nd;
   a.step = step;
   a.inv_nd = 1.0f / (float)nd;
+  a.one = 1.0f;
   return bits == 8 ? run_ring_mode<8>(a, block, st) : run_ring_mode<4>(a, block, st);
 }
 
