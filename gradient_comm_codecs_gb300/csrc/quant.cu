@@ -262,7 +262,8 @@ struct RowWord<16> {
 };
 
 // y = bf16_rn((float)q * s) for every element of every row; BITS == 16
-// copies bf16 rows unchanged.
+// copies bf16 rows unchanged.  The next unit's codes and scales are loaded
+// before the current unit is converted.
 template <int BITS, int LOGB>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) {
   constexpr int K = kQRows;
@@ -272,44 +273,61 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) 
   int64_t u, uend;
   unit_range(a.total_units, (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps, u, uend);
   if (u >= uend) return;
+  struct Row {
+    const uint8_t* c;
+    const float* s;
+    uint16_t* y;
+    bool aligned;
+  };
+  auto row_of = [&](int64_t rw) -> Row {
+    const int64_t src = rw / a.rows_per_src, j = rw - src * a.rows_per_src;
+    Row r;
+    r.c = a.codes[src] + j * a.row_code_bytes;
+    r.s = BITS == 16 ? nullptr : a.scales[src] + j * a.row_blocks;
+    r.y = a.y + rw * a.row_len;
+    r.aligned = ((reinterpret_cast<uintptr_t>(r.c) % sizeof(CW)) |
+                 (reinterpret_cast<uintptr_t>(r.y) & 15)) == 0;
+    return r;
+  };
+  struct Loads {
+    CW w[K];
+    float s[K];
+  };
+  auto load = [&](Loads& l, const Row& r, int64_t e_warp) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int e = k * 256 + lane * 8;
+      l.w[k] = __ldcs(reinterpret_cast<const CW*>(r.c + (((e_warp + e) * BITS) >> 3)));
+      if constexpr (BITS != 16) l.s[k] = __ldg(r.s + ((e_warp + e) >> LOGB));
+    }
+  };
   int64_t row = u / a.units_per_row;
   int64_t t = u - row * a.units_per_row;
-  const uint8_t* crow;
-  const float* srow;
-  uint16_t* yrow;
-  bool row_aligned;
-  auto set_row = [&]() {
-    const int64_t s = row / a.rows_per_src, j = row - s * a.rows_per_src;
-    crow = a.codes[s] + j * a.row_code_bytes;
-    srow = BITS == 16 ? nullptr : a.scales[s] + j * a.row_blocks;
-    yrow = a.y + row * a.row_len;
-    row_aligned = ((reinterpret_cast<uintptr_t>(crow) % sizeof(CW)) |
-                   (reinterpret_cast<uintptr_t>(yrow) & 15)) == 0;
-  };
-  set_row();
+  Row cur_row = row_of(row), nxt_row = cur_row;
+  bool cur_full = cur_row.aligned && a.row_len - t * WE >= WE;
+  Loads cur, nxt;
+  if (cur_full) load(cur, cur_row, t * WE);
   for (; u < uend; ++u) {
+    int64_t rown = row, tn = t + 1;
+    if (tn == a.units_per_row) {
+      tn = 0;
+      ++rown;
+      if (u + 1 < uend) nxt_row = row_of(rown);
+    }
+    const bool nxt_full = u + 1 < uend && nxt_row.aligned && a.row_len - tn * WE >= WE;
+    if (nxt_full) load(nxt, nxt_row, tn * WE);
     const int64_t e_warp = t * WE;
-    const int64_t valid = a.row_len - e_warp;
-    const uint8_t* cw = crow + ((e_warp * BITS) >> 3);
-    uint16_t* yw = yrow + e_warp;
-    if (row_aligned && valid >= WE) {
-      CW w[K];
-      float s[K];
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        const int e = k * 256 + lane * 8;
-        w[k] = __ldcs(reinterpret_cast<const CW*>(cw + ((e * BITS) >> 3)));
-        if constexpr (BITS != 16) s[k] = __ldg(srow + ((e_warp + e) >> LOGB));
-      }
+    uint16_t* yw = cur_row.y + e_warp;
+    if (cur_full) {
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int e = k * 256 + lane * 8;
         if constexpr (BITS == 16) {
-          __stcs(reinterpret_cast<uint4*>(yw + e), w[k]);
+          __stcs(reinterpret_cast<uint4*>(yw + e), cur.w[k]);
         } else {
           float q[8];
-          decode8<BITS>(w[k], q);
-          const float2 s2 = make_float2(s[k], s[k]);
+          decode8<BITS>(cur.w[k], q);
+          const float2 s2 = make_float2(cur.s[k], cur.s[k]);
 #pragma unroll
           for (int i = 0; i < 8; i += 2) {
             const float2 v = mul2(make_float2(q[i], q[i + 1]), s2);
@@ -322,6 +340,8 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) 
         }
       }
     } else {
+      const uint8_t* crow = cur_row.c;
+      const float* srow = cur_row.s;
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int e = k * 256 + lane * 8;
@@ -344,11 +364,11 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) 
         }
       }
     }
-    if (++t == a.units_per_row) {
-      t = 0;
-      ++row;
-      if (u + 1 < uend) set_row();
-    }
+    row = rown;
+    t = tn;
+    cur_row = nxt_row;
+    cur_full = nxt_full;
+    cur = nxt;
   }
 }
 

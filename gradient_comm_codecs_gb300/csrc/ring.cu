@@ -57,40 +57,53 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const RingArgs a) {
   int64_t t = u - r * a.units_per_row;
   const bool has_input = MODE == kRingMiddle || (MODE == kRingLast && a.step > 0);
   int parity = 0;
+  // A rank's row pointers: its own chunk c = (r - 1 - step) mod N_d and the
+  // message of rank r - 1 (r - 1 - step lies in [-N_d, N_d - 2], one wrap).
+  struct Row {
+    const uint16_t* x;
+    const uint8_t* c;
+    const float* s;
+  };
+  auto row_of = [&](int64_t rr) -> Row {
+    const int32_t ri = (int32_t)rr;
+    int32_t c = ri - 1 - a.step;
+    if (c < 0) c += a.nd;
+    const int32_t prev = ri == 0 ? a.nd - 1 : ri - 1;
+    if (!has_input) return {a.x + rr * a.bucket + (int64_t)c * a.L, nullptr, nullptr};
+    return {a.x + rr * a.bucket + (int64_t)c * a.L, a.codes_in + (int64_t)prev * a.cb,
+            a.scales_in + (int64_t)prev * a.nb};
+  };
   // The next unit's loads are issued before the current unit is computed.
   struct Loads {
     uint4 x[K];
     CW c[K];
     float s[K];
   };
-  auto load = [&](Loads& l, int64_t rr, int64_t tt) {
-    const int64_t c = ((rr - 1 - a.step) % a.nd + a.nd) % a.nd;
-    const int64_t prev = (rr - 1 + a.nd) % a.nd;
-    const uint16_t* xrow = a.x + rr * a.bucket + c * a.L;
-    const uint8_t* crow = a.codes_in + prev * a.cb;
-    const float* srow = a.scales_in + prev * a.nb;
+  auto load = [&](Loads& l, const Row& row, int64_t tt) {
     const int64_t ew = tt * G::U + (int64_t)wsub * G::kWarpElems;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const int64_t e = ew + k * 256 + lane * 8;
       if (e < a.L) {
-        l.x[k] = __ldcs(reinterpret_cast<const uint4*>(xrow + e));
+        l.x[k] = __ldcs(reinterpret_cast<const uint4*>(row.x + e));
         if (has_input) {
-          l.c[k] = __ldcs(reinterpret_cast<const CW*>(crow + ((e * BITS) >> 3)));
-          l.s[k] = __ldg(srow + (e >> LOGB));
+          l.c[k] = __ldcs(reinterpret_cast<const CW*>(row.c + ((e * BITS) >> 3)));
+          l.s[k] = __ldg(row.s + (e >> LOGB));
         }
       }
     }
   };
+  Row cur_row = row_of(r), nxt_row = cur_row;
   Loads cur, nxt;
-  load(cur, r, t);
+  load(cur, cur_row, t);
   for (; u < uend; ++u, parity ^= 1) {
     int64_t rn = r, tn = t + 1;
     if (tn == a.units_per_row) {
       tn = 0;
       ++rn;
+      if (u + 1 < uend) nxt_row = row_of(rn);
     }
-    if (u + 1 < uend) load(nxt, rn, tn);
+    if (u + 1 < uend) load(nxt, nxt_row, tn);
     const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;
     const int64_t valid = a.L - e_warp;  // a multiple of 64 when positive
     float v[K][8];
@@ -128,6 +141,7 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const RingArgs a) {
     r = rn;
     t = tn;
     cur = nxt;
+    cur_row = nxt_row;
   }
 }
 
