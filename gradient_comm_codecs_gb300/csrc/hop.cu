@@ -164,15 +164,8 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
         for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(acc[k][i]));
         am[k] = m;
       }
-      warp_block_absmax<G>(am);
-      if constexpr (WPB > 1) {
-        const float m = group_absmax<WPB>(am[0], red, parity, warp, gid, lane);
-#pragma unroll
-        for (int k = 0; k < K; ++k) am[k] = m;
-      }
       Scale sc[NSC];
-#pragma unroll
-      for (int i = 0; i < NSC; ++i) sc[i] = make_scale<QMAX>(am[i * RPB]);
+      block_scales<G, QMAX>(am, sc, red, parity, warp, gid, lane);
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int e = k * 256 + lane * 8;
@@ -325,15 +318,8 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
         const float m3 = fmaxf(fabsf(acc[k][6]), fabsf(acc[k][7]));
         am[k] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
       }
-      warp_block_absmax<G>(am);
-      if constexpr (WPB > 1) {
-        const float m = group_absmax<WPB>(am[0], red, parity, warp, gid, lane);
-#pragma unroll
-        for (int k = 0; k < K; ++k) am[k] = m;
-      }
       Scale sc[NSC];
-#pragma unroll
-      for (int i = 0; i < NSC; ++i) sc[i] = make_scale<QMAX>(am[i * RPB]);
+      block_scales<G, QMAX>(am, sc, red, parity, warp, gid, lane);
       uint8_t* co = a.codes_out + ((obase * BITS) >> 3) + lane * (8 * BITS / 8);
 #pragma unroll
       for (int k = 0; k < K; ++k) {
@@ -372,15 +358,8 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
           const float m3 = fmaxf(fabsf(pq[k][6]), fabsf(pq[k][7]));
           am[k] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
         }
-        warp_block_absmax<G>(am);
-        if constexpr (WPB > 1) {
-          const float m = group_absmax<WPB>(am[0], red, parity, warp, gid, lane);
-#pragma unroll
-          for (int k = 0; k < K; ++k) am[k] = m;
-        }
         Scale sc[NSC];
-#pragma unroll
-        for (int i = 0; i < NSC; ++i) sc[i] = make_scale<127>(am[i * RPB]);
+        block_scales<G, 127>(am, sc, red, parity, warp, gid, lane);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
           uint32_t c[8];
