@@ -59,7 +59,7 @@ struct HopCfg {
   // the requantizing modes need whole blocks per warp group; plain final hops do not
   static constexpr int WPB = (MODE == kRequant || MODE == kFinalAdamQwz) ? G::WPB : 1;
   static constexpr int U = WPB * G::kWarpElems;
-  static constexpr int SCH = BITS == 4 ? 4 : 2;                // sources per load chunk
+  static constexpr int SCH = (BITS == 4 && G::NSC == 1) ? 4 : 2;  // sources per load chunk
 };
 
 template <int BITS, int K, int NSC, int SCH>
@@ -214,14 +214,15 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
 // WIDE (fixed at compile time, so the loads of the next chunk schedule
 // freely around the state accesses): grad_out and the Adam state move as one
 // 256-bit access per lane; the launcher picks it when they are 32-byte aligned.
-template <int BITS, int MODE, int LOGB, bool WIDE>
+//
+// SCH: sources per load chunk (two chunks in flight).  Four for the final
+// modes of int4 messages with more than two sources, else two; the launcher
+// picks it from the source count.
+template <int BITS, int MODE, int LOGB, bool WIDE, int SCH>
 __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a) {
   using C = HopCfg<BITS, MODE, LOGB>;
   using G = typename C::G;
   constexpr int K = C::K, WPB = C::WPB, NSC = G::NSC, RPB = G::RPB;
-  // requant: two sources per chunk (registers); final hops: the state loads
-  // need deeper prefetch, four int4 sources per chunk
-  constexpr int SCH = (MODE == kRequant || BITS == 8) ? 2 : 4;
   constexpr int QMAX = (1 << (BITS - 1)) - 1;
   constexpr int GPC = kWarps / WPB;
   constexpr int ROWB = 256 * BITS / 8;  // code bytes of one 256-element row
@@ -394,14 +395,26 @@ cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
     const int64_t groups = kWarps / C::WPB;
     const int64_t ctas = (a.total_units + groups - 1) / groups;
     const bool tiled = a.R % C::U == 0;
+    // four sources a chunk pays off for int4 final hops with many sources
+    constexpr bool kWideChunk = MODE != kRequant && BITS == 4;
+    const bool wide_chunk = kWideChunk && a.S > 2;
+    auto launch_tiled = [&](auto w, auto sch) {
+      constexpr bool W = decltype(w)::value;
+      constexpr int S = decltype(sch)::value;
+      const void* k = reinterpret_cast<const void*>(&hop_tiled_kernel<BITS, MODE, LOGB, W, S>);
+      hop_tiled_kernel<BITS, MODE, LOGB, W, S><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+    };
+    using Two = std::integral_constant<int, 2>;
+    using Four = std::integral_constant<int, kWideChunk ? 4 : 2>;
     if (tiled && (MODE == kRequant || a.wide)) {
-      constexpr bool W = MODE != kRequant;
-      const void* k = reinterpret_cast<const void*>(&hop_tiled_kernel<BITS, MODE, LOGB, W>);
-      hop_tiled_kernel<BITS, MODE, LOGB, W><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+      using W = std::integral_constant<bool, MODE != kRequant>;
+      if (wide_chunk) launch_tiled(W{}, Four{});
+      else launch_tiled(W{}, Two{});
     } else if constexpr (MODE == kFinalAdamQwz) {
       if (!tiled) return cudaErrorNotSupported;
-      const void* k = reinterpret_cast<const void*>(&hop_tiled_kernel<BITS, MODE, LOGB, false>);
-      hop_tiled_kernel<BITS, MODE, LOGB, false><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+      using W = std::integral_constant<bool, false>;
+      if (wide_chunk) launch_tiled(W{}, Four{});
+      else launch_tiled(W{}, Two{});
     } else {  // ragged rows, or fp32 arrays only 16-byte aligned
       const void* k = reinterpret_cast<const void*>(&hop_kernel<BITS, MODE, LOGB>);
       hop_kernel<BITS, MODE, LOGB><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
