@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kThreads) adam_kernel(const AdamArgs a) {
       }
 #pragma unroll
       for (int k = 0; k < kAdamRows; ++k)
-        adam_apply8(g[k], s[k], base + k * 256, a.master, a.m, a.v, a.param, a.ac, WIDE);
+        adam_apply8<true>(g[k], s[k], base + k * 256, a.master, a.m, a.v, a.param, a.ac, WIDE);
     } else {
 #pragma unroll
       for (int k = 0; k < kAdamRows; ++k) {
@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(kThreads) adam_kernel(const AdamArgs a) {
 cudaError_t launch_adam(const float* grad, int64_t n, const AdamConstsHost& ac, float* master,
                         float* m, float* v, uint16_t* param, cudaStream_t st) {
   AdamArgs a{grad, master, m, v, param, n,
-             AdamConsts{ac.lr, ac.beta1, ac.beta2, ac.eps, ac.omb1, ac.omb2, ac.bc1, ac.bc2}};
+             AdamConsts{ac.lr, ac.beta1, ac.beta2, ac.eps, ac.omb1, ac.omb2, ac.bc1, ac.bc2,
+                        ac.rbc1, ac.rbc2, 1.0f}};
   const int64_t units = (n + kAdamUnit - 1) / kAdamUnit;
   const int64_t ctas = (units + kWarps - 1) / kWarps;
   if (aligned32(grad) && aligned32(master) && aligned32(m) && aligned32(v)) {

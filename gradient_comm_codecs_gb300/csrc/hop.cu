@@ -442,8 +442,8 @@ cudaError_t launch_hop_reduce(const HopLaunch& h, cudaStream_t st) {
   a.scales_out = h.scales_out;
   a.grad_out = h.grad_out;
   a.inv_nd = h.inv_nd;
-  a.ac = AdamConsts{h.ac.lr, h.ac.beta1, h.ac.beta2, h.ac.eps,
-                    h.ac.omb1, h.ac.omb2, h.ac.bc1, h.ac.bc2};
+  a.ac = AdamConsts{h.ac.lr,   h.ac.beta1, h.ac.beta2, h.ac.eps, h.ac.omb1, h.ac.omb2,
+                    h.ac.bc1,  h.ac.bc2,   h.ac.rbc1,  h.ac.rbc2, 1.0f};
   a.master = h.master;
   a.m = h.m;
   a.v = h.v;

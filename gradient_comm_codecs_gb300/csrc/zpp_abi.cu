@@ -53,6 +53,14 @@ zpp_status adam_consts(const zpp_adam_hparams* hp, AdamConstsHost* ac) {
   ac->bc2 = (float)(1.0 - pow_by_squaring((double)hp->beta2, hp->step));
   ac->omb1 = (float)(1.0 - (double)hp->beta1);
   ac->omb2 = (float)(1.0 - (double)hp->beta2);
+  // RN(1/bc): the double quotient rounded to float is the correctly rounded
+  // float reciprocal, double rounding being innocuous for a quotient when the
+  // wider format has at least 2p + 2 bits (53 >= 2*24 + 2).
+  auto rcp = [](float bc) {
+    return (bc >= 0x1p-40f && bc <= 1.0f) ? (float)(1.0 / (double)bc) : 0.0f;
+  };
+  ac->rbc1 = rcp(ac->bc1);
+  ac->rbc2 = rcp(ac->bc2);
   return ZPP_OK;
 }
 

@@ -12,6 +12,7 @@ constexpr int kThreads = 256;  // threads per CTA of every kernel
 
 struct AdamConstsHost {
   float lr, beta1, beta2, eps, omb1, omb2, bc1, bc2;
+  float rbc1, rbc2;  // RN(1 / bc) when bc is in [2^-40, 1], else 0
 };
 
 // Row-blocked quantization of bf16 rows.

@@ -8,14 +8,19 @@
 //      x drawn three ways: within 3 ulps of every (k + 1/2) s, |k| <= Q (the
 //      rounding boundaries), uniform in [-m, m], and those values truncated to
 //      bf16; 2^33 draws of 8 values each per divisor.
+//  (float)(1.0 / (double)d) == __frcp_rn(d)   for every float d in [2^-40, 1]
+//      (the host's reciprocal of the Adam bias corrections; exhaustive)
+//  div2_bc(x, d, RN(1/d)) == __fdiv_rn(x, d)   for seeded d in [2^-40, 1] and x
+//      drawn near the rounding boundaries of x/d, log-uniform over [2^-120, 2^100],
+//      and zero; 2^32 draws of 2 values each.
 #include <cstdio>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "zpp_device.cuh"
 
-__device__ unsigned long long g_bad[4];
-__device__ unsigned int g_first[4];
+__device__ unsigned long long g_bad[6];
+__device__ unsigned int g_first[6];
 
 __global__ void check_div(uint32_t lo, uint32_t hi) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -92,21 +97,68 @@ __global__ void check_quant(uint64_t n) {
   }
 }
 
+__global__ void check_rcp(uint32_t lo, uint32_t hi) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t b = lo + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; b <= hi; b += stride) {
+    const float d = __uint_as_float((uint32_t)b);
+    if ((float)(1.0 / (double)d) != __frcp_rn(d)) {
+      if (atomicAdd(&g_bad[4], 1ull) == 0) g_first[4] = (uint32_t)b;
+    }
+  }
+}
+
+__global__ void check_bcdiv(uint64_t n) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += stride) {
+    uint32_t h = mix((uint32_t)t ^ mix((uint32_t)(t >> 32) + 0x51ed270bu));
+    const float d = ldexpf(1.0f + (float)(h >> 9) * (1.0f / 8388608.0f), -(int)(h % 41u));
+    const float dd = d > 1.0f ? 1.0f : d;
+    const float rd = (float)(1.0 / (double)dd);
+    float x[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      h = mix(h + 0x9e3779b9u * (uint32_t)(i + 1));
+      const uint32_t kind = h & 3u;
+      float v;
+      if (kind == 0) {  // next to a rounding boundary of x / d: x = RN(q d) +- a few ulps
+        const float q = ldexpf(1.0f + (float)(h >> 9) * (1.0f / 8388608.0f),
+                               (int)((h >> 2) % 200u) - 100);
+        v = __int_as_float(__float_as_int(__fmul_rn(q, dd)) + (int)((h >> 27) % 7u) - 3);
+      } else if (kind == 1) {
+        v = ldexpf(1.0f + (float)(h >> 9) * (1.0f / 8388608.0f), (int)((h >> 2) % 220u) - 120);
+      } else if (kind == 2) {
+        v = 0.0f;
+      } else {
+        v = ldexpf(1.0f + (float)(h >> 9) * (1.0f / 8388608.0f), (int)((h >> 2) % 60u) - 40);
+      }
+      x[i] = (h >> 31) ? -v : v;
+    }
+    const float2 q = zpp::div2_bc(make_float2(x[0], x[1]), dd, rd);
+    if (q.x != __fdiv_rn(x[0], dd) || q.y != __fdiv_rn(x[1], dd)) {
+      if (atomicAdd(&g_bad[5], 1ull) == 0) g_first[5] = __float_as_uint(x[0]);
+    }
+  }
+}
+
 int main() {
-  unsigned long long zero[4] = {0, 0, 0, 0};
+  unsigned long long zero[6] = {0, 0, 0, 0, 0, 0};
   if (cudaMemcpyToSymbol(g_bad, zero, sizeof zero) != cudaSuccess) return 2;
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
   check_div<<<sms * 8, 256>>>(0u, 0x7F800000u);  // +0 .. largest finite
   check_quant<<<sms * 8, 256>>>(1ull << 33);
+  check_rcp<<<sms * 8, 256>>>(0x2B800000u, 0x3F800000u);  // 2^-40 .. 1
+  check_bcdiv<<<sms * 8, 256>>>(1ull << 32);
   if (cudaDeviceSynchronize() != cudaSuccess) return 3;
-  unsigned long long bad[4];
-  unsigned int first[4];
+  unsigned long long bad[6];
+  unsigned int first[6];
   cudaMemcpyFromSymbol(bad, g_bad, sizeof bad);
   cudaMemcpyFromSymbol(first, g_first, sizeof first);
   printf("div_qmax7 %llu %08x\n", bad[0], bad[0] ? first[0] : 0u);
   printf("div_qmax127 %llu %08x\n", bad[1], bad[1] ? first[1] : 0u);
   printf("quantize_q7 %llu %08x\n", bad[2], bad[2] ? first[2] : 0u);
   printf("quantize_q127 %llu %08x\n", bad[3], bad[3] ? first[3] : 0u);
+  printf("bias_rcp %llu %08x\n", bad[4], bad[4] ? first[4] : 0u);
+  printf("bias_div %llu %08x\n", bad[5], bad[5] ? first[5] : 0u);
   return 0;
 }

@@ -3,7 +3,9 @@ IEEE divisions: the block scale absmax/qmax by reciprocal + one FMA correction
 equals the IEEE quotient for every non-negative float (both bit widths,
 exhaustive), and the quantizer's FMA-division codes equal rint of the IEEE
 quotient on 2^33 seeded draws of 8 values per bit width, most of them within
-3 ulps of a rounding boundary."""
+3 ulps of a rounding boundary; the Adam bias-correction reciprocal and FMA
+division equal the IEEE ones (exhaustive over the divisors, 2^32 seeded
+dividend pairs)."""
 import os
 import subprocess
 
@@ -25,5 +27,5 @@ def test_exhaustive_device_identities(tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stdout + out.stderr
     res = {line.split()[0]: int(line.split()[1]) for line in out.stdout.splitlines()}
-    assert res == {"div_qmax7": 0, "div_qmax127": 0, "quantize_q7": 0, "quantize_q127": 0}, \
-        out.stdout
+    assert res == {"div_qmax7": 0, "div_qmax127": 0, "quantize_q7": 0, "quantize_q127": 0,
+                   "bias_rcp": 0, "bias_div": 0}, out.stdout
