@@ -41,18 +41,18 @@ NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 KERNEL_OF = {  # launch name -> CUDA kernel (for the roofline and the ncu summaries)
-    "qwz_quant": "quant_tiled_kernel<BITS, false, LOGB>",
+    "qwz_quant": "quant_tiled_kernel<BITS, false, LOGB, false>",
     "qwz_dequant": "dequant_kernel<BITS, LOGB>",
-    "qgz_reorder_quant": "quant_tiled_kernel<BITS, true, LOGB>",
-    "qgz_hop1": "hop_tiled_kernel<BITS, kRequant, LOGB>",
-    "qgz_final_hop": "hop_tiled_kernel<BITS, kFinalAdam, LOGB>",
-    "qgz_final_hop_qwz": "hop_tiled_kernel<BITS, kFinalAdamQwz, LOGB>",
+    "qgz_reorder_quant": "quant_tiled_kernel<BITS, true, LOGB, false>",
+    "qgz_hop1": "hop_tiled_kernel<BITS, kRequant, LOGB, false, 2>",
+    "qgz_final_hop": "hop_tiled_kernel<BITS, kFinalAdam, LOGB, WIDE, SCH>",
+    "qgz_final_hop_qwz": "hop_tiled_kernel<BITS, kFinalAdamQwz, LOGB, WIDE, SCH>",
     "grad_accumulate": "accumulate_kernel",
+    "qgz_reorder_quant_acc": "quant_tiled_kernel<BITS, true, LOGB, true>",
     "shard_adam": "adam_kernel<WIDE>",
     "hpz_gather": "dequant_kernel<BITS, LOGB> (G secondary sources)",
     "ring_step": "ring_kernel<BITS, LOGB, MODE>",
     "ring_adam": "adam_kernel<WIDE>",
-    "qgz_reorder_quant_acc": "quant_tiled_kernel<BITS, true, LOGB, true>",
 }
 KERNEL_SRC = {"qwz_quant": "quant.cu", "qwz_dequant": "quant.cu", "qgz_reorder_quant": "quant.cu",
               "qgz_hop1": "hop.cu", "qgz_final_hop": "hop.cu", "qgz_final_hop_qwz": "hop.cu",
