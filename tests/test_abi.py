@@ -150,3 +150,65 @@ def test_binding_rejects_host_tensors():
     x = torch.zeros(1024, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         Z.zpp_qwz_quant(x, 1, 1024, 256, 8, x, x, stream=0)
+
+
+def test_next_rows_validation(lib):
+    """The Adam -> qwZ hop, accumulation, hpZ and ring entry points reject bad
+    arguments on the host, before anything is enqueued."""
+    from gradient_comm_codecs_gb300._lib import zpp_adam_hparams, zpp_adam_state
+    P = ctypes.c_void_p
+    ref = ctypes.byref
+    hp = zpp_adam_hparams(1e-4, 0.9, 0.999, 1e-8, 1)
+    st = zpp_adam_state(A, A, A, A)
+    # Adam -> qwZ fused final hop
+    f = lib.zpp_qgz_final_hop_adam_qwz
+    b = 4 * 512
+    assert f(1, P(A), P(A), 1, 4, b, 256, 4, None, None, ref(st), 8, P(A), P(A), None) == 1
+    assert f(1, P(A), P(A), 1, 4, b, 256, 4, None, ref(hp), None, 8, P(A), P(A), None) == 1
+    assert f(1, P(A), P(A), 2, 2, b, 256, 4, None, ref(hp), ref(st), 8, P(A), P(A), None) == 1
+    assert f(1, P(A), P(A), 1, 4, b, 256, 4, None, ref(hp), ref(st), 4, P(A), P(A), None) == 3
+    assert f(1, P(A), P(A), 1, 4, 4 * 768, 256, 4, None, ref(hp), ref(st), 8, P(A), P(A),
+             None) == 3                                             # L = 768: not a multiple of 512
+    assert f(1, P(A), P(A), 1, 4, b, 256, 4, None, ref(hp), ref(st), 8, P(M), P(A), None) == 2
+    # gradient accumulation
+    g = lib.zpp_grad_accumulate
+    assert g(P(A), P(A), 100, 2, None) == 1
+    assert g(P(A), P(A), -1, 1, None) == 1
+    assert g(None, P(A), 100, 1, None) == 1
+    assert g(P(A), P(M), 100, 1, None) == 2
+    assert g(None, None, 0, 1, None) == 0
+    r = lib.zpp_qgz_reorder_quant_acc
+    assert r(P(A), P(A), 2, 2, 4 * 256 + 4, 256, 4, P(A), P(A), None) == 1
+    assert r(P(A), None, 2, 2, 4096, 256, 4, P(A), P(A), None) == 1
+    assert r(P(A), P(M), 2, 2, 4096, 256, 4, P(A), P(A), None) == 2
+    assert r(None, None, 2, 2, 0, 256, 4, None, None, None) == 0
+    # hpZ
+    two = (ctypes.c_void_p * 2)(A, A)
+    mis = (ctypes.c_void_p * 2)(A, M)
+    h = lib.zpp_hpz_gather
+    C = lambda arr: ctypes.cast(arr, ctypes.c_void_p)   # noqa: E731
+    assert h(0, 1, 4096, 256, 8, C(two), C(two), P(A), None) == 1
+    assert h(65, 1, 4096, 256, 8, C(two), C(two), P(A), None) == 1
+    assert h(2, 0, 4096, 256, 8, C(two), C(two), P(A), None) == 1
+    assert h(2, 1, 4096, 100, 8, C(two), C(two), P(A), None) == 1
+    assert h(2, 1, 4095, 256, 4, C(two), C(two), P(A), None) == 1
+    assert h(2, 1, 4096, 256, 8, C(two), None, P(A), None) == 1
+    assert h(2, 1, 4096, 256, 8, C(mis), C(two), P(A), None) == 2
+    assert h(2, 1, 4096, 256, 8, C(two), C(two), P(M), None) == 2
+    assert h(2, 1, 0, 256, 8, None, None, None, None) == 0
+    assert lib.zpp_hpz_secondary_bytes(2, 4096, 256, 8) == 2 * (4096 + 4 * 16)
+    assert lib.zpp_hpz_secondary_bytes(2, 4096, 256, 4) == 2 * (2048 + 4 * 16)
+    assert lib.zpp_hpz_secondary_bytes(2, 4096, 256, 16) == 2 * 2 * 4096
+    assert lib.zpp_hpz_secondary_bytes(2, 4096, 256, 5) == -1
+    assert lib.zpp_hpz_secondary_bytes(0, 4096, 256, 8) == -1
+    # ring
+    q = lib.zpp_ring_rs_step
+    bb = 4 * 256
+    assert q(4, 4, bb, 64, 8, P(A), P(A), P(A), P(A), P(A), P(A), None) == 1    # step >= N_d
+    assert q(-1, 4, bb, 64, 8, P(A), P(A), P(A), P(A), P(A), P(A), None) == 1
+    assert q(1, 4, bb + 64, 64, 8, P(A), P(A), P(A), P(A), P(A), P(A), None) == 1
+    assert q(1, 4, bb, 64, 8, P(A), None, P(A), P(A), P(A), None, None) == 1    # middle: input
+    assert q(0, 4, bb, 64, 8, P(A), None, None, None, P(A), None, None) == 1    # first: output
+    assert q(3, 4, bb, 64, 8, P(A), P(A), P(A), None, None, None, None) == 1    # last: gradient
+    assert q(3, 4, bb, 64, 8, P(A), P(A), P(A), None, None, P(M), None) == 2
+    assert q(0, 4, 0, 64, 8, None, None, None, None, None, None, None) == 0
