@@ -332,36 +332,90 @@ class CodecPath:
             self.run_standalone_adam(stream, adam_step, mark)
 
     def run_from_host(self, w_host=None, grads_host=None, param_host=None, stream=None,
-                      adam_step: int | None = None, sa_grad_host=None, sa_param_host=None):
+                      adam_step: int | None = None, sa_grad_host=None, sa_param_host=None,
+                      copy_streams: int = 2):
         """One pass on host-resident data: copy this step's weights and
-        gradients in (pinned host tensors, asynchronous on `stream`), run, and
-        copy the updated 16-bit parameters back.  `grads_host` is one tensor,
-        or one per micro-batch; `sa_grad_host`/`sa_param_host` are the
-        standalone shard's fp32 gradients in and bf16 parameters out.  Returns
-        the bytes moved each way (h2d, d2h)."""
+        gradients in from pinned host tensors, run, and copy the updated
+        16-bit parameters back.  `grads_host` is one tensor, or one per
+        micro-batch; `sa_grad_host`/`sa_param_host` are the standalone shard's
+        fp32 gradients in and bf16 parameters out.
+
+        The copies are split into chunks over `copy_streams` streams each way
+        and overlap the kernels: the qwZ kernels start once the weights are in
+        while the gradients are still arriving, and the next call's inputs may
+        start arriving as soon as this call's kernels have read theirs, under
+        this call's read-back.  Returns the bytes moved each way (h2d, d2h)."""
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        n_cs = max(1, int(copy_streams))
+        if getattr(self, "_copy_in", None) is None or len(self._copy_in) != n_cs:
+            self._copy_in = [torch.cuda.Stream(self.device) for _ in range(n_cs)]
+            self._copy_out = [torch.cuda.Stream(self.device) for _ in range(n_cs)]
+            self._inputs_free = None
+        cin, cout = self._copy_in, self._copy_out
         h2d = d2h = 0
-        with torch.cuda.stream(s):
-            if w_host is not None:
-                self.w.copy_(w_host, non_blocking=True)
-                h2d += w_host.numel() * w_host.element_size()
-            if grads_host is not None:
-                hosts = grads_host if isinstance(grads_host, (list, tuple)) else [grads_host]
-                if len(hosts) != self.microbatches:
-                    raise ValueError("grads_host: one tensor per micro-batch")
-                for dst, src in zip(self.grads_mb, hosts):
-                    dst.copy_(src, non_blocking=True)
-                    h2d += src.numel() * src.element_size()
-            if sa_grad_host is not None:
-                self.sa_grad.copy_(sa_grad_host, non_blocking=True)
-                h2d += sa_grad_host.numel() * sa_grad_host.element_size()
-            self.run(s.cuda_stream, adam_step)
-            if param_host is not None:
-                src = self.param if self.param is not None else self.master
-                param_host.copy_(src, non_blocking=True)
-                d2h += param_host.numel() * param_host.element_size()
-            if sa_param_host is not None:
-                src = self.sa_param if self.sa_param is not None else self.sa_master
-                sa_param_host.copy_(src, non_blocking=True)
-                d2h += sa_param_host.numel() * sa_param_host.element_size()
+
+        def after(stream_from, streams_to):
+            ev = torch.cuda.Event()
+            ev.record(stream_from)
+            for t in streams_to:
+                t.wait_event(ev)
+            return ev
+
+        def split_copy(pairs, streams):
+            """Copy every (dst, src) pair in chunks round-robin over `streams`;
+            returns the bytes copied."""
+            nbytes, i = 0, 0
+            for dst, src in pairs:
+                n = src.numel()
+                nbytes += n * src.element_size()
+                step = max(1 << 20, -(-n // len(streams)))
+                for lo in range(0, n, step):
+                    with torch.cuda.stream(streams[i % len(streams)]):
+                        dst[lo:lo + step].copy_(src[lo:lo + step], non_blocking=True)
+                    i += 1
+            return nbytes
+
+        # the input buffers are free once the previous call's kernels have read them
+        if self._inputs_free is None:
+            after(s, cin)
+        else:
+            for c in cin:
+                c.wait_event(self._inputs_free)
+        if w_host is not None:
+            h2d += split_copy([(self.w, w_host)], cin)
+            for c in cin:
+                after(c, [s])
+        if self.qwz is not None:
+            self.run_qwz(s.cuda_stream)
+        if self.hpz:
+            self.run_hpz(s.cuda_stream)
+        pairs = []
+        if grads_host is not None:
+            hosts = grads_host if isinstance(grads_host, (list, tuple)) else [grads_host]
+            if len(hosts) != self.microbatches:
+                raise ValueError("grads_host: one tensor per micro-batch")
+            pairs += list(zip(self.grads_mb, hosts))
+        if sa_grad_host is not None:
+            pairs.append((self.sa_grad, sa_grad_host))
+        if pairs:
+            h2d += split_copy(pairs, cin)
+            for c in cin:
+                after(c, [s])
+        if self.qgz is not None:
+            self.run_qgz(s.cuda_stream, adam_step)
+        if self.standalone_adam:
+            self.run_standalone_adam(s.cuda_stream, adam_step)
+        self._inputs_free = torch.cuda.Event()
+        self._inputs_free.record(s)
+        back = []
+        if param_host is not None:
+            back.append((param_host, self.param if self.param is not None else self.master))
+        if sa_param_host is not None:
+            back.append((sa_param_host, self.sa_param if self.sa_param is not None
+                         else self.sa_master))
+        if back:
+            after(s, cout)
+            d2h += split_copy(back, cout)
+            for c in cout:  # the next step's Adam must not overwrite them before
+                after(c, [s])
         return h2d, d2h

@@ -667,3 +667,49 @@ def test_ring_arguments():
     with pytest.raises(Z.ZppError) as e:
         Z.zpp_ring_rs_step(1, 2, 512, 64, 8, x, c, s, None, None, g[1:])
     assert e.value.status == Z.ZPP_ERR_MISALIGNED
+
+
+# ---- the end-to-end call on host buffers ---------------------------------------------------------
+
+@pytest.mark.parametrize("copy_streams", [1, 3])
+def test_run_from_host(copy_streams):
+    """CodecPath.run_from_host (chunked copies over several streams overlapping
+    the kernels): the parameters copied back are the oracle's, with
+    micro-batches, hpZ and a standalone shard in the pass."""
+    Z = zpp()
+    from gradient_comm_codecs_gb300 import AdamSpec, CodecPath, QgzSpec, QwzSpec
+    from gpu_helpers import grads_for
+    wl = W.TINY
+    q, g = wl.qwz, wl.qgz
+    n_sa = 50001
+    path = CodecPath(QwzSpec(q.nranks, q.shard, q.block, q.bits, nodes=g.nodes),
+                     QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits), AdamSpec(),
+                     device="cuda", keep_grad=True, microbatches=2, standalone_adam=n_sa, hpz=True)
+    w = synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, q.phi).pin_memory()
+    mbs = [grads_for(g, wl.seed, microbatch=k).pin_memory() for k in range(2)]
+    master0 = synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, g.bucket).float()
+    path.master.copy_(master0)
+    sg = torch.from_numpy((RNG.standard_normal(n_sa) * 1e-3).astype(np.float32)).pin_memory()
+    sp = (RNG.standard_normal(n_sa) * 0.02).astype(np.float32)
+    path.sa_master.copy_(torch.from_numpy(sp))
+    p_host = torch.empty(g.bucket, dtype=torch.bfloat16).pin_memory()
+    sa_host = torch.empty(n_sa, dtype=torch.bfloat16).pin_memory()
+    h2d, d2h = path.run_from_host(w, mbs, p_host, adam_step=1, sa_grad_host=sg,
+                                  sa_param_host=sa_host, copy_streams=copy_streams)
+    torch.cuda.synchronize()
+    assert h2d == 2 * q.phi + 2 * 2 * g.nd * g.bucket + 4 * n_sa
+    assert d2h == 2 * g.bucket + 2 * n_sa
+    c, s = oracle.qwz_quant(u16(w), q.nranks, q.shard, q.block, q.bits)
+    assert_bytes_equal(u16(path.w_full), oracle.qwz_dequant(c, s, q.nranks, q.shard, q.block,
+                                                            q.bits), "weights gathered (hpZ)")
+    acc = oracle.grad_accumulate([u16(t) for t in mbs])
+    c1, s1 = oracle.qgz_reorder_quant_f32(acc, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+    c2, s2 = oracle.qgz_hop1(c1, s1, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+    gref = oracle.qgz_hop2(c2, s2, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+    a = wl.adam
+    z = np.zeros(g.bucket, np.float32)
+    _, _, _, pb = oracle.adam_step(gref, master0.numpy(), z, z, a.lr, a.beta1, a.beta2, a.eps, 1)
+    assert_bf16_ulp(u16(p_host), pb, "parameters copied back")
+    zs = np.zeros(n_sa, np.float32)
+    _, _, _, qb = oracle.adam_step(sg.numpy(), sp, zs, zs, a.lr, a.beta1, a.beta2, a.eps, 1)
+    assert_bf16_ulp(u16(sa_host), qb, "standalone parameters copied back")
