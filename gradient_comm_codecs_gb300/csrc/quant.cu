@@ -293,12 +293,19 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) 
     CW w[K];
     float s[K];
   };
+  // lane-invariant offsets: the lane's code bytes and each row's scale within a unit
+  constexpr int ROWB = 256 * BITS / 8;
+  const int lane_code = lane * 8 * BITS / 8;
+  int soff[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) soff[k] = (k * 256 + lane * 8) >> LOGB;
   auto load = [&](Loads& l, const Row& r, int64_t e_warp) {
+    const uint8_t* cw = r.c + ((e_warp * BITS) >> 3) + lane_code;
+    const float* sw = r.s + (e_warp >> LOGB);
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-      const int e = k * 256 + lane * 8;
-      l.w[k] = __ldcs(reinterpret_cast<const CW*>(r.c + (((e_warp + e) * BITS) >> 3)));
-      if constexpr (BITS != 16) l.s[k] = __ldg(r.s + ((e_warp + e) >> LOGB));
+      l.w[k] = __ldcs(reinterpret_cast<const CW*>(cw + k * ROWB));
+      if constexpr (BITS != 16) l.s[k] = __ldg(sw + soff[k]);
     }
   };
   int64_t row = u / a.units_per_row;
@@ -319,11 +326,11 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) 
     const int64_t e_warp = t * WE;
     uint16_t* yw = cur_row.y + e_warp;
     if (cur_full) {
+      uint16_t* yl = yw + lane * 8;
 #pragma unroll
       for (int k = 0; k < K; ++k) {
-        const int e = k * 256 + lane * 8;
         if constexpr (BITS == 16) {
-          __stcs(reinterpret_cast<uint4*>(yw + e), cur.w[k]);
+          __stcs(reinterpret_cast<uint4*>(yl + k * 256), cur.w[k]);
         } else {
           float q[8];
           decode8<BITS>(cur.w[k], q);
@@ -334,7 +341,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const DequantArgs a) 
             q[i] = v.x;
             q[i + 1] = v.y;
           }
-          __stcs(reinterpret_cast<uint4*>(yw + e),
+          __stcs(reinterpret_cast<uint4*>(yl + k * 256),
                  make_uint4(pack_bf16x2(q[0], q[1]), pack_bf16x2(q[2], q[3]),
                             pack_bf16x2(q[4], q[5]), pack_bf16x2(q[6], q[7])));
         }
