@@ -166,6 +166,9 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
       }
       Scale sc[NSC];
       block_scales<G, QMAX>(am, sc, red, parity, warp, gid, lane);
+      // R is a multiple of B, so obase mod B = e_warp mod B
+      const int ew_mod = (int)(e_warp & (G::B - 1));
+      float* so = a.scales_out + (obase >> LOGB);
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int e = k * 256 + lane * 8;
@@ -173,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 2) hop_kernel(const HopArgs a) {
         quantize8<QMAX>(acc[k], sc[k / RPB], c);
         if (!on[k]) continue;
         *reinterpret_cast<CW*>(a.codes_out + (((obase + e) * BITS) >> 3)) = pack8<BITS>(c);
-        if (((e_warp + e) & (G::B - 1)) == 0) a.scales_out[(obase + e) >> LOGB] = sc[k / RPB].s;
+        if (((ew_mod + e) & (G::B - 1)) == 0) so[(ew_mod + e) >> LOGB] = sc[k / RPB].s;
       }
     } else {
 #pragma unroll
@@ -322,13 +325,16 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
       Scale sc[NSC];
       block_scales<G, QMAX>(am, sc, red, parity, warp, gid, lane);
       uint8_t* co = a.codes_out + ((obase * BITS) >> 3) + lane * (8 * BITS / 8);
+      // R is a multiple of B, so obase mod B = e_warp mod B
+      const int ew_mod = (int)(e_warp & (G::B - 1));
+      float* so = a.scales_out + (obase >> LOGB);
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         uint32_t c[8];
         quantize8<QMAX>(acc[k], sc[k / RPB], c);
         *reinterpret_cast<CW*>(co + k * ROWB) = pack8<BITS>(c);
         const int e = k * 256 + lane * 8;
-        if (((e_warp + e) & (G::B - 1)) == 0) a.scales_out[(obase + e) >> LOGB] = sc[k / RPB].s;
+        if (((ew_mod + e) & (G::B - 1)) == 0) so[(ew_mod + e) >> LOGB] = sc[k / RPB].s;
       }
     } else {
       const float2 inv = make_float2(a.inv_nd, a.inv_nd);
@@ -361,13 +367,15 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
         }
         Scale sc[NSC];
         block_scales<G, 127>(am, sc, red, parity, warp, gid, lane);
+        const int ew_mod = (int)(e_warp & (G::B - 1));  // = obase mod B
+        float* qs = a.qwz_scales + (obase >> LOGB);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
           uint32_t c[8];
           quantize8<127>(pq[k], sc[k / RPB], c);
           const int e = k * 256 + lane * 8;
           *reinterpret_cast<uint2*>(a.qwz_codes + obase + e) = pack_i8x8(c);
-          if (((e_warp + e) & (G::B - 1)) == 0) a.qwz_scales[(obase + e) >> LOGB] = sc[k / RPB].s;
+          if (((ew_mod + e) & (G::B - 1)) == 0) qs[(ew_mod + e) >> LOGB] = sc[k / RPB].s;
         }
       }
     }
