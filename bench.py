@@ -44,7 +44,7 @@ KERNEL_OF = {  # launch name -> CUDA kernel (for the roofline and the ncu summar
     "qwz_quant": "quant_tiled_kernel<BITS, false, LOGB, false>",
     "qwz_dequant": "dequant_kernel<BITS, LOGB>",
     "qgz_reorder_quant": "quant_tiled_kernel<BITS, true, LOGB, false>",
-    "qgz_hop1": "hop_tiled_kernel<BITS, kRequant, LOGB, false, 2>",
+    "qgz_hop1": "hop1_kernel<BITS, LOGB, SCH>",
     "qgz_final_hop": "hop_tiled_kernel<BITS, kFinalAdam, LOGB, WIDE, SCH>",
     "qgz_final_hop_qwz": "hop_tiled_kernel<BITS, kFinalAdamQwz, LOGB, WIDE, SCH>",
     "grad_accumulate": "accumulate_kernel",

@@ -392,6 +392,176 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
   }
 }
 
+// Hop 1 of a two-hop topology (dequantize, sum the G sources of the node in
+// rank order, requantize), laid out for the sum: a lane owns 32 consecutive
+// elements of the warp's 1024, so one source costs it one 16-byte code load
+// (int4; two for int8) and one scale load, and a block of B <= 1024 elements
+// is B/32 neighbouring lanes.  (Messages start 16-byte aligned and every
+// source, row and unit offset is a multiple of 1024 elements, so each lane's
+// code vector is 16-byte aligned.)
+//
+// Sources are read SCH at a time in two register chunks, the next chunk in
+// flight while the current one is summed; the next unit's first chunk is
+// loaded while the last chunk of this unit is summed, so the loads never
+// drain between units.  Requires S to be a multiple of 2*SCH.
+//
+// int4 chunks whose scales are all below 2^-5 (a warp vote) are dequantized
+// by one FMA a code (dequant_acc_i4); others by the magic-number decode.
+template <int BITS, int LOGB, int SCH>
+__global__ void __launch_bounds__(kThreads, 2) hop1_kernel(const HopArgs a) {
+  using G = Geo<LOGB, 4>;
+  constexpr int WPB = G::WPB, GPC = kWarps / WPB;
+  constexpr int QMAX = (1 << (BITS - 1)) - 1;
+  constexpr int LB = G::B >= 1024 ? 32 : G::B / 32;  // lanes sharing a block within a warp
+  constexpr int LCB = 32 * BITS / 8;                 // code bytes of a lane's 32 elements
+  constexpr unsigned kAll = 0xffffffffu;
+  struct Chunk {
+    uint32_t w[SCH][BITS];  // 32 codes a source
+    float s[SCH];
+  };
+  __shared__ float red[2][kWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = warp / WPB, wsub = warp - gid * WPB;
+
+  int64_t u, uend;
+  unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
+  if (u >= uend) return;
+  const int64_t d0 = u / a.units_per_row;
+  int64_t t = u - d0 * a.units_per_row;
+  int32_t dn = (int32_t)(d0 / a.G), dl = (int32_t)(d0 - (int64_t)dn * a.G);
+  const int64_t cstep = (a.in_rank_elems * BITS) >> 3;  // bytes between consecutive sources
+  const int64_t fstep = a.in_rank_elems >> LOGB;        // scales between consecutive sources
+  const int lane_e = 32 * lane;                         // the lane's first element in the slab
+  // lane's code and scale pointers of unit (dn, dl, t), source 0 (node dn's first rank)
+  auto bases = [&](int32_t n, int32_t l, int64_t tt, const uint8_t*& cp, const float*& sp) {
+    const int64_t e0 = (int64_t)n * a.G * a.in_rank_elems + (int64_t)l * a.R + tt * G::U +
+                       (int64_t)wsub * G::kWarpElems;
+    cp = a.codes_in + ((e0 * BITS) >> 3) + lane * LCB;
+    sp = a.scales_in + ((e0 + lane_e) >> LOGB);
+  };
+  auto load = [&](Chunk& ch, const uint8_t* cp, const float* sp, int s0) {
+#pragma unroll
+    for (int j = 0; j < SCH; ++j) {
+      const uint4* src = reinterpret_cast<const uint4*>(cp + (int64_t)(s0 + j) * cstep);
+#pragma unroll
+      for (int h = 0; h < BITS / 4; ++h) {
+        const uint4 v = __ldcs(src + h);
+        ch.w[j][4 * h] = v.x;
+        ch.w[j][4 * h + 1] = v.y;
+        ch.w[j][4 * h + 2] = v.z;
+        ch.w[j][4 * h + 3] = v.w;
+      }
+      ch.s[j] = __ldg(sp + (int64_t)(s0 + j) * fstep);
+    }
+  };
+  float acc[4][8];
+  const float2 one2 = make_float2(a.one, a.one);
+  auto sum = [&](const Chunk& ch) {
+    bool fma_path = false;
+    if constexpr (BITS == 4) {
+      float smax = ch.s[0];
+#pragma unroll
+      for (int j = 1; j < SCH; ++j) smax = fmaxf(smax, ch.s[j]);
+      fma_path = __all_sync(kAll, smax < kI4FmaMaxScale);
+    }
+    if (fma_path) {
+#pragma unroll
+      for (int j = 0; j < SCH; ++j) {
+        const I4Fma k = i4_fma_scale(ch.s[j]);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) dequant_acc_i4(ch.w[j][m], k, one2, acc[m]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < SCH; ++j) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float q[8];
+          if constexpr (BITS == 4) decode8<4>(ch.w[j][m], q);
+          else decode8<8>(make_uint2(ch.w[j][2 * m], ch.w[j][2 * m + 1]), q);
+          accumulate8(acc[m], q, ch.s[j], a.one);
+        }
+      }
+    }
+  };
+
+  const uint8_t* cp;
+  const float* sp;
+  bases(dn, dl, t, cp, sp);
+  Chunk ca, cb;
+  load(ca, cp, sp, 0);
+  int parity = 0;
+  for (; u < uend; ++u, parity ^= 1) {
+    int64_t tn = t + 1;
+    int32_t dnn = dn, dln = dl;
+    if (tn == a.units_per_row) {
+      tn = 0;
+      if (++dln == a.G) {
+        dln = 0;
+        ++dnn;
+      }
+    }
+    const bool more = u + 1 < uend;
+    const uint8_t* cpn;
+    const float* spn;
+    bases(dnn, dln, tn, cpn, spn);
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[m][i] = 0.0f;
+    for (int c = 0; c < a.S; c += 2 * SCH) {
+      load(cb, cp, sp, c + SCH);
+      sum(ca);
+      if (c + 2 * SCH < a.S) load(ca, cp, sp, c + 2 * SCH);
+      else if (more) load(ca, cpn, spn, 0);
+      sum(cb);
+    }
+
+    // requantize the lane's 32 sums with its block's scale
+    float m0 = 0.0f, m1 = 0.0f, m2 = 0.0f, m3 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      m0 = fmaxf(m0, fabsf(acc[0][i]));
+      m1 = fmaxf(m1, fabsf(acc[1][i]));
+      m2 = fmaxf(m2, fabsf(acc[2][i]));
+      m3 = fmaxf(m3, fabsf(acc[3][i]));
+    }
+    float am = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+#pragma unroll
+    for (int o = 1; o < LB; o <<= 1) am = fmaxf(am, __shfl_xor_sync(kAll, am, o));
+    if constexpr (WPB > 1) am = group_absmax<WPB>(am, red, parity, warp, gid, lane);
+    const Scale sc = make_scale<QMAX>(am);
+    const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;
+    const int64_t obase = ((int64_t)dn * a.G + dl) * a.R + e_warp;
+    uint32_t out[BITS];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      uint32_t c[8];
+      quantize8<QMAX>(acc[m], sc, c);
+      if constexpr (BITS == 4) {
+        out[m] = pack_i4x8(c);
+      } else {
+        const uint2 p = pack_i8x8(c);
+        out[2 * m] = p.x;
+        out[2 * m + 1] = p.y;
+      }
+    }
+    uint4* co = reinterpret_cast<uint4*>(a.codes_out + ((obase * BITS) >> 3) + lane * LCB);
+#pragma unroll
+    for (int h = 0; h < BITS / 4; ++h)
+      co[h] = make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+    // R is a multiple of B, so obase mod B = e_warp mod B
+    const int eb = (int)(e_warp & (G::B - 1)) + lane_e;
+    if ((eb & (G::B - 1)) == 0) a.scales_out[(obase >> LOGB) + (eb >> LOGB)] = sc.s;
+
+    t = tn;
+    dn = dnn;
+    dl = dln;
+    cp = cpn;
+    sp = spn;
+  }
+}
+
 template <int BITS, int MODE>
 cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
   return dispatch_logb(block, [&](auto lb) -> cudaError_t {
@@ -412,6 +582,18 @@ cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
       const void* k = reinterpret_cast<const void*>(&hop_tiled_kernel<BITS, MODE, LOGB, W, S>);
       hop_tiled_kernel<BITS, MODE, LOGB, W, S><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
     };
+    if constexpr (MODE == kRequant) {
+      if (tiled && a.S % 4 == 0) {  // sources in pairs of chunks of 2 or 4
+        auto launch1 = [&](auto sch) {
+          constexpr int S = decltype(sch)::value;
+          const void* k = reinterpret_cast<const void*>(&hop1_kernel<BITS, LOGB, S>);
+          hop1_kernel<BITS, LOGB, S><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+        };
+        if (BITS == 4 && a.S % 8 == 0) launch1(std::integral_constant<int, BITS == 4 ? 4 : 2>{});
+        else launch1(std::integral_constant<int, 2>{});
+        return cudaGetLastError();
+      }
+    }
     using Two = std::integral_constant<int, 2>;
     using Four = std::integral_constant<int, kWideChunk ? 4 : 2>;
     if (tiled && (MODE == kRequant || a.wide)) {

@@ -13,14 +13,17 @@
 //  div2_bc(x, d, RN(1/d)) == __fdiv_rn(x, d)   for seeded d in [2^-40, 1] and x
 //      drawn near the rounding boundaries of x/d, log-uniform over [2^-120, 2^100],
 //      and zero; 2^32 draws of 2 values each.
+//  dequant_acc_i4(w, i4_fma_scale(s), 1, acc) == acc + fl(q * s), each rounded,
+//      for all 16 int4 codes q and every float s in [0, 2^-5) (exhaustive), with
+//      acc a seeded value of the scale's magnitude (the one-FMA int4 dequantization)
 #include <cstdio>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "zpp_device.cuh"
 
-__device__ unsigned long long g_bad[6];
-__device__ unsigned int g_first[6];
+__device__ unsigned long long g_bad[7];
+__device__ unsigned int g_first[7];
 
 __global__ void check_div(uint32_t lo, uint32_t hi) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -140,8 +143,36 @@ __global__ void check_bcdiv(uint64_t n) {
   }
 }
 
+__global__ void check_i4fma(uint32_t lo, uint32_t hi) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t b = lo + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; b < hi; b += stride) {
+    const float s = __uint_as_float((uint32_t)b);
+    const zpp::I4Fma k = zpp::i4_fma_scale(s);
+    const uint32_t h = mix((uint32_t)b);
+    // an accumulator of the scale's size, either sign
+    const float a0 = __fmul_rn(s, (float)((int)(h >> 8) - (1 << 23)) * (1.0f / 1048576.0f));
+    const float2 one2 = make_float2(1.0f, 1.0f);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      // codes q = -8..-1 (nibbles 8..15) then 0..7, element e in nibble e
+      const uint32_t w = half == 0 ? 0xFEDCBA98u : 0x76543210u;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = a0;
+      zpp::dequant_acc_i4(w, k, one2, acc);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int q = half == 0 ? e - 8 : e;
+        if (acc[e] != __fadd_rn(a0, __fmul_rn((float)q, s))) {
+          if (atomicAdd(&g_bad[6], 1ull) == 0) g_first[6] = (uint32_t)b;
+        }
+      }
+    }
+  }
+}
+
 int main() {
-  unsigned long long zero[6] = {0, 0, 0, 0, 0, 0};
+  unsigned long long zero[7] = {0, 0, 0, 0, 0, 0, 0};
   if (cudaMemcpyToSymbol(g_bad, zero, sizeof zero) != cudaSuccess) return 2;
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
@@ -149,9 +180,10 @@ int main() {
   check_quant<<<sms * 8, 256>>>(1ull << 33);
   check_rcp<<<sms * 8, 256>>>(0x2B800000u, 0x3F800000u);  // 2^-40 .. 1
   check_bcdiv<<<sms * 8, 256>>>(1ull << 32);
+  check_i4fma<<<sms * 8, 256>>>(0u, 0x3D000000u);  // +0 .. just below 2^-5
   if (cudaDeviceSynchronize() != cudaSuccess) return 3;
-  unsigned long long bad[6];
-  unsigned int first[6];
+  unsigned long long bad[7];
+  unsigned int first[7];
   cudaMemcpyFromSymbol(bad, g_bad, sizeof bad);
   cudaMemcpyFromSymbol(first, g_first, sizeof first);
   printf("div_qmax7 %llu %08x\n", bad[0], bad[0] ? first[0] : 0u);
@@ -160,5 +192,6 @@ int main() {
   printf("quantize_q127 %llu %08x\n", bad[3], bad[3] ? first[3] : 0u);
   printf("bias_rcp %llu %08x\n", bad[4], bad[4] ? first[4] : 0u);
   printf("bias_div %llu %08x\n", bad[5], bad[5] ? first[5] : 0u);
+  printf("i4_fma %llu %08x\n", bad[6], bad[6] ? first[6] : 0u);
   return 0;
 }

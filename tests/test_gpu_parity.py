@@ -162,6 +162,44 @@ def test_qgz_chain(bits, block, N, G):
     assert_f32_bitexact(g, want, "reduced gradient (bit-exact by construction)")
 
 
+def hop1_input(N, G, block, bits, L, rng):
+    """One-shot messages of Student-t gradients (scales well below 2^-5) with
+    outlier, all-zero and subnormal-scale blocks mixed in, so that both int4
+    dequantization paths of hop 1 (one FMA a code when every scale of a chunk
+    is below 2^-5, the magic-number decode otherwise) run in one launch."""
+    Nd = N * G
+    bucket = Nd * L
+    x = (rng.standard_t(3, Nd * bucket) * 1e-3).astype(np.float32)
+    nb = Nd * bucket // block
+    xb = x.reshape(nb, block)
+    xb[::37] *= 100.0                         # scales above 2^-5
+    xb[5::41] = 0.0                           # zero scales
+    xb[11::43] = rng.integers(-500, 500, size=xb[11::43].shape) * 2.0 ** -140  # subnormal scales
+    c1, s1 = oracle.qgz_reorder_quant(oracle.f32_to_bf16(x), N, G, bucket, block, bits)
+    return bucket, c1, s1
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("block", [64, 256, 512, 2048])
+@pytest.mark.parametrize("N,G", [(2, 4), (2, 8), (3, 8)])
+def test_hop1_whole_unit_slices(bits, block, N, G):
+    """Hop 1 where every destination row is whole 1024-element warp units and
+    G is a multiple of four (the per-lane 32-element kernel), against the oracle."""
+    Z = zpp()
+    L = 2 * max(1024, block)
+    bucket, c1, s1 = hop1_input(N, G, block, bits, L, RNG)
+    c2, s2 = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
+    nl = N * L
+    Nd = N * G
+    out_c = torch.full((Nd * Z.zpp_codes_bytes(nl, bits),), 0x5A, dtype=torch.uint8, device="cuda")
+    out_s = torch.full((Nd * (nl // block),), float("nan"), device="cuda")
+    Z.zpp_qgz_hop_reduce(1, torch.from_numpy(c1).cuda(), torch.from_numpy(s1).cuda(), N, G,
+                         bucket, block, bits, codes_out=out_c, scales_out=out_s)
+    torch.cuda.synchronize()
+    assert_bytes_equal(np_bytes(out_c), c2, "hop-1 codes")
+    assert_f32_bitexact(np_f32(out_s), s2, "hop-1 scales")
+
+
 def test_slice_permutation_through_the_message():
     """The permutation is read back from the message itself: rank r's slice j,
     filled with a constant that identifies (r, j), must be found at position
