@@ -331,9 +331,41 @@ class CodecPath:
         if self.standalone_adam:
             self.run_standalone_adam(stream, adam_step, mark)
 
+    def _bind_input_set(self, k: int, n_sets: int, names=("w", "grads_mb", "sa_grad")):
+        """Point the inputs in `names` (of w / grads_mb / sa_grad; grads
+        follows grads_mb) at device input set k of n_sets.  Set 0 is the
+        path's own buffers; the others are allocated on first use."""
+        if getattr(self, "_sets", None) is None or len(self._sets) != n_sets:
+            own = {"w": getattr(self, "w", None), "grads_mb": getattr(self, "grads_mb", None),
+                   "sa_grad": getattr(self, "sa_grad", None)}
+            if getattr(self, "_sets", None):
+                own = self._sets[0]
+            self._sets = [own]
+            for _ in range(1, n_sets):
+                self._sets.append({
+                    "w": torch.empty_like(own["w"]) if own["w"] is not None else None,
+                    "grads_mb": [torch.empty_like(t) for t in own["grads_mb"]]
+                    if own["grads_mb"] is not None else None,
+                    "sa_grad": torch.empty_like(own["sa_grad"]) if own["sa_grad"] is not None
+                    else None})
+            self._last_read = {}  # (set, input) -> event after the kernels that last read it
+            self._bound = {"w": 0, "grads_mb": 0, "sa_grad": 0}
+            self._next_set = 0
+        b = self._sets[k]
+        if "w" in names and b["w"] is not None:
+            self.w = b["w"]
+            self._bound["w"] = k
+        if "grads_mb" in names and b["grads_mb"] is not None:
+            self.grads_mb = b["grads_mb"]
+            self.grads = self.grads_mb[-1]
+            self._bound["grads_mb"] = k
+        if "sa_grad" in names and b["sa_grad"] is not None:
+            self.sa_grad = b["sa_grad"]
+            self._bound["sa_grad"] = k
+
     def run_from_host(self, w_host=None, grads_host=None, param_host=None, stream=None,
                       adam_step: int | None = None, sa_grad_host=None, sa_param_host=None,
-                      copy_streams: int = 2):
+                      copy_streams: int = 2, input_sets: int = 2):
         """One pass on host-resident data: copy this step's weights and
         gradients in from pinned host tensors, run, and copy the updated
         16-bit parameters back.  `grads_host` is one tensor, or one per
@@ -342,16 +374,31 @@ class CodecPath:
 
         The copies are split into chunks over `copy_streams` streams each way
         and overlap the kernels: the qwZ kernels start once the weights are in
-        while the gradients are still arriving, and the next call's inputs may
-        start arriving as soon as this call's kernels have read theirs, under
-        this call's read-back.  Returns the bytes moved each way (h2d, d2h)."""
+        while the gradients are still arriving.  Successive calls take turns
+        over `input_sets` sets of device input buffers (weights, gradients,
+        standalone gradients), so with two or more sets the next call's
+        inputs start arriving as soon as this call's have, under this call's
+        kernels and read-back; a set is refilled only once the kernels of the
+        call that last used it have read it.  After the call, `w`, `grads_mb`,
+        `grads` and `sa_grad` are that call's device inputs (those not copied
+        in stay where they were).  Returns the bytes moved each way
+        (h2d, d2h)."""
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         n_cs = max(1, int(copy_streams))
+        n_sets = max(1, int(input_sets))
         if getattr(self, "_copy_in", None) is None or len(self._copy_in) != n_cs:
             self._copy_in = [torch.cuda.Stream(self.device) for _ in range(n_cs)]
             self._copy_out = [torch.cuda.Stream(self.device) for _ in range(n_cs)]
-            self._inputs_free = None
         cin, cout = self._copy_in, self._copy_out
+        if getattr(self, "_sets", None) is None or len(self._sets) != n_sets:
+            self._bind_input_set(0, n_sets, ())
+        k = self._next_set
+        self._next_set = (k + 1) % n_sets
+        # only the inputs this call copies in move to set k; the kernels read the rest
+        # where the caller left them
+        copied = [n for n, h in (("w", w_host), ("grads_mb", grads_host), ("sa_grad", sa_grad_host))
+                  if h is not None]
+        self._bind_input_set(k, n_sets, copied)
         h2d = d2h = 0
 
         def after(stream_from, streams_to):
@@ -375,12 +422,14 @@ class CodecPath:
                     i += 1
             return nbytes
 
-        # the input buffers are free once the previous call's kernels have read them
-        if self._inputs_free is None:
-            after(s, cin)
-        else:
-            for c in cin:
-                c.wait_event(self._inputs_free)
+        # a buffer of set k is refilled once the kernels that last read it are done
+        for n in copied:
+            ev = self._last_read.get((k, n))
+            if ev is None:
+                after(s, cin)
+            else:
+                for c in cin:
+                    c.wait_event(ev)
         if w_host is not None:
             h2d += split_copy([(self.w, w_host)], cin)
             for c in cin:
@@ -405,8 +454,10 @@ class CodecPath:
             self.run_qgz(s.cuda_stream, adam_step)
         if self.standalone_adam:
             self.run_standalone_adam(s.cuda_stream, adam_step)
-        self._inputs_free = torch.cuda.Event()
-        self._inputs_free.record(s)
+        read = torch.cuda.Event()
+        read.record(s)
+        for n, j in self._bound.items():
+            self._last_read[(j, n)] = read
         back = []
         if param_host is not None:
             back.append((param_host, self.param if self.param is not None else self.master))

@@ -751,3 +751,43 @@ def test_run_from_host(copy_streams):
     zs = np.zeros(n_sa, np.float32)
     _, _, _, qb = oracle.adam_step(sg.numpy(), sp, zs, zs, a.lr, a.beta1, a.beta2, a.eps, 1)
     assert_bf16_ulp(u16(sa_host), qb, "standalone parameters copied back")
+
+
+@pytest.mark.parametrize("input_sets", [1, 2, 3])
+def test_run_from_host_successive_steps(input_sets):
+    """Three run_from_host calls in a row with different weights and gradients
+    each, over 1-3 sets of device input buffers (the next call's copies in
+    flight under this call's kernels): after the third call the gathered
+    weights, the reduced gradient and the parameters copied back are the
+    oracle's for the third step, with m and v carried over three Adam steps."""
+    Z = zpp()
+    from gradient_comm_codecs_gb300 import AdamSpec, CodecPath, QgzSpec, QwzSpec
+    from gpu_helpers import grads_for
+    wl = W.TINY
+    q, g = wl.qwz, wl.qgz
+    a = wl.adam
+    path = CodecPath(QwzSpec(q.nranks, q.shard, q.block, q.bits),
+                     QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits), AdamSpec(),
+                     device="cuda", keep_grad=True)
+    master0 = synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, g.bucket).float()
+    path.master.copy_(master0)
+    ws = [synth.fill(W.WEIGHT_RECIPE, 10 + k, synth.WEIGHTS, 0, q.phi).pin_memory()
+          for k in range(3)]
+    gs = [grads_for(g, wl.seed, microbatch=k).pin_memory() for k in range(3)]
+    p_host = torch.empty(g.bucket, dtype=torch.bfloat16).pin_memory()
+    for k in range(3):
+        path.run_from_host(ws[k], gs[k], p_host, adam_step=1 + k, input_sets=input_sets)
+    torch.cuda.synchronize()
+    c, s = oracle.qwz_quant(u16(ws[2]), q.nranks, q.shard, q.block, q.bits)
+    assert_bytes_equal(u16(path.w_full), oracle.qwz_dequant(c, s, q.nranks, q.shard, q.block,
+                                                            q.bits), "third step's weights")
+    p, m, v = master0.numpy(), np.zeros(g.bucket, np.float32), np.zeros(g.bucket, np.float32)
+    for k in range(3):
+        c1, s1 = oracle.qgz_reorder_quant(u16(gs[k]), g.nodes, g.gpus_per_node, g.bucket,
+                                          g.block, g.bits)
+        c2, s2 = oracle.qgz_hop1(c1, s1, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+        gref = oracle.qgz_hop2(c2, s2, g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
+        p, m, v, pb = oracle.adam_step(gref, p, m, v, a.lr, a.beta1, a.beta2, a.eps, 1 + k)
+    assert_f32_bitexact(np_f32(path.grad_out), gref, "third step's reduced gradient")
+    assert_rel_close(np_f32(path.master), p, 1e-5, "master after three steps")
+    assert_bf16_ulp(u16(p_host), pb, "parameters copied back after three steps")
