@@ -51,7 +51,7 @@ KERNEL_OF = {  # launch name -> CUDA kernel (for the roofline and the ncu summar
     "qgz_reorder_quant_acc": "quant_tiled_kernel<BITS, true, LOGB, true>",
     "shard_adam": "adam_kernel<WIDE>",
     "hpz_gather": "dequant_kernel<BITS, LOGB> (G secondary sources)",
-    "ring_step": "ring_kernel<BITS, LOGB, MODE>",
+    "ring_step": "ring1_kernel<BITS, LOGB, MODE, WIDE>",
     "ring_adam": "adam_kernel<WIDE>",
 }
 KERNEL_SRC = {"qwz_quant": "quant.cu", "qwz_dequant": "quant.cu", "qgz_reorder_quant": "quant.cu",

@@ -145,6 +145,174 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const RingArgs a) {
   }
 }
 
+// Whole-unit chunks (L a multiple of the unit): a lane owns 32 consecutive
+// elements of its warp's 1024, as in the hop-1 kernel.  Per unit it loads 64
+// bytes of its own bf16 chunk (two 32-byte vectors when WIDE: whole sectors per
+// request), one code vector (16 bytes int4, 32 int8) and one scale of the
+// incoming message; a block of B <= 1024 elements is B/32 neighbouring lanes.
+// The next unit's loads are in flight while the current one is computed.
+//
+// int4 units whose incoming scales are all below 2^-5 (a warp vote) are
+// dequantized by one FMA a code (dequant_acc_i4); others by the magic-number
+// decode.  WIDE: x and grad_out 32-byte aligned.
+template <int BITS, int LOGB, int MODE, bool WIDE>
+__global__ void __launch_bounds__(kThreads, 2) ring1_kernel(const RingArgs a) {
+  using G = Geo<LOGB, kRingRows>;
+  constexpr int WPB = G::WPB, GPC = kWarps / WPB;
+  constexpr int QMAX = (1 << (BITS - 1)) - 1;
+  constexpr int LB = G::B >= 1024 ? 32 : G::B / 32;  // lanes sharing a block within a warp
+  constexpr int CV = BITS / 4;                       // 16-byte code vectors of a lane
+  constexpr unsigned kAll = 0xffffffffu;
+  __shared__ float red[2][kWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = warp / WPB, wsub = warp - gid * WPB;
+  int64_t u, uend;
+  unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
+  if (u >= uend) return;  // the whole group shares the range
+  int64_t r = u / a.units_per_row;
+  int64_t t = u - r * a.units_per_row;
+  const bool has_input = MODE == kRingMiddle || (MODE == kRingLast && a.step > 0);
+  const int64_t e_lane = (int64_t)wsub * G::kWarpElems + 32 * lane;  // lane's element in tile 0
+  // rank rr's pointers at tile 0: its own chunk c = (rr - 1 - step) mod N_d and the
+  // message of rank rr - 1
+  struct Row {
+    const float* x;  // bf16 pairs, read as 32-bit words
+    const uint8_t* c;
+    const float* s;
+  };
+  auto row_of = [&](int64_t rr) -> Row {
+    const int32_t ri = (int32_t)rr;
+    int32_t c = ri - 1 - a.step;
+    if (c < 0) c += a.nd;
+    const int32_t prev = ri == 0 ? a.nd - 1 : ri - 1;
+    Row w;
+    w.x = reinterpret_cast<const float*>(a.x + rr * a.bucket + (int64_t)c * a.L + e_lane);
+    w.c = has_input ? a.codes_in + (int64_t)prev * a.cb + ((e_lane * BITS) >> 3) : nullptr;
+    w.s = has_input ? a.scales_in + (int64_t)prev * a.nb + (e_lane >> LOGB) : nullptr;
+    return w;
+  };
+  struct Loads {
+    float x[16];  // 32 bf16
+    uint32_t c[BITS];
+    float s;
+  };
+  auto load = [&](Loads& l, const Row& w, int64_t tt) {
+    const int64_t eo = tt * G::U;
+    float (&x0)[8] = *reinterpret_cast<float(*)[8]>(&l.x[0]);
+    float (&x1)[8] = *reinterpret_cast<float(*)[8]>(&l.x[8]);
+    ld8_cs(w.x + eo / 2, WIDE, x0);
+    ld8_cs(w.x + eo / 2 + 8, WIDE, x1);
+    if (has_input) {
+      const uint4* cp = reinterpret_cast<const uint4*>(w.c + ((eo * BITS) >> 3));
+#pragma unroll
+      for (int h = 0; h < CV; ++h) {
+        const uint4 v = __ldcs(cp + h);
+        l.c[4 * h] = v.x;
+        l.c[4 * h + 1] = v.y;
+        l.c[4 * h + 2] = v.z;
+        l.c[4 * h + 3] = v.w;
+      }
+      l.s = __ldg(w.s + (eo >> LOGB));
+    }
+  };
+
+  const float2 one2 = make_float2(a.one, a.one);
+  Row cur_row = row_of(r), nxt_row = cur_row;
+  Loads cur, nxt;
+  load(cur, cur_row, t);
+  int parity = 0;
+  for (; u < uend; ++u, parity ^= 1) {
+    int64_t rn = r, tn = t + 1;
+    if (tn == a.units_per_row) {
+      tn = 0;
+      ++rn;
+      if (u + 1 < uend) nxt_row = row_of(rn);
+    }
+    if (u + 1 < uend) load(nxt, nxt_row, tn);
+
+    float v[4][8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w = __float_as_uint(cur.x[4 * m + i]);
+        v[m][2 * i] = bf16_lo(w);
+        v[m][2 * i + 1] = bf16_hi(w);
+      }
+    if (has_input) {  // own + D(msg), each rounded
+      bool fma_path = false;
+      if constexpr (BITS == 4) fma_path = __all_sync(kAll, cur.s < kI4FmaMaxScale);
+      if (fma_path) {
+        if constexpr (BITS == 4) {
+          const I4Fma k = i4_fma_scale(cur.s);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) dequant_acc_i4(cur.c[m], k, one2, v[m]);
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float q[8];
+          if constexpr (BITS == 4) decode8<4>(cur.c[m], q);
+          else decode8<8>(make_uint2(cur.c[2 * m], cur.c[2 * m + 1]), q);
+          accumulate8(v[m], q, cur.s, a.one);
+        }
+      }
+    }
+    const int64_t e = t * G::U + e_lane;  // the lane's first element within the chunk
+    if constexpr (MODE == kRingLast) {
+      float* go = a.grad_out + r * a.L + e;
+      const float2 inv = make_float2(a.inv_nd, a.inv_nd);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        float g[8];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const float2 p = mul2(make_float2(v[m][i], v[m][i + 1]), inv);
+          g[i] = p.x;
+          g[i + 1] = p.y;
+        }
+        st8_cs(go + 8 * m, WIDE, g);
+      }
+    } else {  // requantize the lane's 32 values with its block's scale
+      float m0 = 0.0f, m1 = 0.0f, m2 = 0.0f, m3 = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        m0 = fmaxf(m0, fabsf(v[0][i]));
+        m1 = fmaxf(m1, fabsf(v[1][i]));
+        m2 = fmaxf(m2, fabsf(v[2][i]));
+        m3 = fmaxf(m3, fabsf(v[3][i]));
+      }
+      float am = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+#pragma unroll
+      for (int o = 1; o < LB; o <<= 1) am = fmaxf(am, __shfl_xor_sync(kAll, am, o));
+      if constexpr (WPB > 1) am = group_absmax<WPB>(am, red, parity, warp, gid, lane);
+      const Scale sc = make_scale<QMAX>(am);
+      uint32_t out[BITS];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t c[8];
+        quantize8<QMAX>(v[m], sc, c);
+        if constexpr (BITS == 4) {
+          out[m] = pack_i4x8(c);
+        } else {
+          const uint2 p = pack_i8x8(c);
+          out[2 * m] = p.x;
+          out[2 * m + 1] = p.y;
+        }
+      }
+      uint4* co = reinterpret_cast<uint4*>(a.codes_out + r * a.cb + ((e * BITS) >> 3));
+#pragma unroll
+      for (int h = 0; h < CV; ++h)
+        co[h] = make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+      if ((e & (G::B - 1)) == 0) a.scales_out[r * a.nb + (e >> LOGB)] = sc.s;
+    }
+    r = rn;
+    t = tn;
+    cur = nxt;
+    cur_row = nxt_row;
+  }
+}
+
 template <int BITS, int MODE>
 cudaError_t run_ring(RingArgs a, int block, cudaStream_t st) {
   return dispatch_logb(block, [&](auto lb) -> cudaError_t {
@@ -153,9 +321,21 @@ cudaError_t run_ring(RingArgs a, int block, cudaStream_t st) {
     a.units_per_row = (a.L + G::U - 1) / G::U;
     a.total_units = (int64_t)a.nd * a.units_per_row;
     const int64_t groups = kWarps / G::WPB;
+    const int64_t ctas = (a.total_units + groups - 1) / groups;
+    if (a.L % G::U == 0) {  // whole-unit chunks
+      auto launch1 = [&](auto w) {
+        constexpr bool W = decltype(w)::value;
+        const void* k = reinterpret_cast<const void*>(&ring1_kernel<BITS, LOGB, MODE, W>);
+        ring1_kernel<BITS, LOGB, MODE, W><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+      };
+      if (aligned32(a.x) && (!a.grad_out || aligned32(a.grad_out)))
+        launch1(std::integral_constant<bool, true>{});
+      else
+        launch1(std::integral_constant<bool, false>{});
+      return cudaGetLastError();
+    }
     const void* k = reinterpret_cast<const void*>(&ring_kernel<BITS, LOGB, MODE>);
-    ring_kernel<BITS, LOGB, MODE>
-        <<<grid_for(k, (a.total_units + groups - 1) / groups), kThreads, 0, st>>>(a);
+    ring_kernel<BITS, LOGB, MODE><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
     return cudaGetLastError();
   });
 }
