@@ -412,7 +412,6 @@ __global__ void __launch_bounds__(kThreads, 2) hop1_kernel(const HopArgs a) {
   using G = Geo<LOGB, 4>;
   constexpr int WPB = G::WPB, GPC = kWarps / WPB;
   constexpr int QMAX = (1 << (BITS - 1)) - 1;
-  constexpr int LB = G::B >= 1024 ? 32 : G::B / 32;  // lanes sharing a block within a warp
   constexpr int LCB = 32 * BITS / 8;                 // code bytes of a lane's 32 elements
   constexpr unsigned kAll = 0xffffffffu;
   struct Chunk {
@@ -465,23 +464,17 @@ __global__ void __launch_bounds__(kThreads, 2) hop1_kernel(const HopArgs a) {
       fma_path = __all_sync(kAll, smax < kI4FmaMaxScale);
     }
     if (fma_path) {
+      if constexpr (BITS == 4) {
 #pragma unroll
-      for (int j = 0; j < SCH; ++j) {
-        const I4Fma k = i4_fma_scale(ch.s[j]);
+        for (int j = 0; j < SCH; ++j) {
+          const I4Fma k = i4_fma_scale(ch.s[j]);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) dequant_acc_i4(ch.w[j][m], k, one2, acc[m]);
+          for (int m = 0; m < 4; ++m) dequant_acc_i4(ch.w[j][m], k, one2, acc[m]);
+        }
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < SCH; ++j) {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          float q[8];
-          if constexpr (BITS == 4) decode8<4>(ch.w[j][m], q);
-          else decode8<8>(make_uint2(ch.w[j][2 * m], ch.w[j][2 * m + 1]), q);
-          accumulate8(acc[m], q, ch.s[j], a.one);
-        }
-      }
+      for (int j = 0; j < SCH; ++j) lane32_dequant_acc<BITS>(ch.w[j], ch.s[j], false, a.one, acc);
     }
   };
 
@@ -518,38 +511,10 @@ __global__ void __launch_bounds__(kThreads, 2) hop1_kernel(const HopArgs a) {
     }
 
     // requantize the lane's 32 sums with its block's scale
-    float m0 = 0.0f, m1 = 0.0f, m2 = 0.0f, m3 = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      m0 = fmaxf(m0, fabsf(acc[0][i]));
-      m1 = fmaxf(m1, fabsf(acc[1][i]));
-      m2 = fmaxf(m2, fabsf(acc[2][i]));
-      m3 = fmaxf(m3, fabsf(acc[3][i]));
-    }
-    float am = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-#pragma unroll
-    for (int o = 1; o < LB; o <<= 1) am = fmaxf(am, __shfl_xor_sync(kAll, am, o));
-    if constexpr (WPB > 1) am = group_absmax<WPB>(am, red, parity, warp, gid, lane);
-    const Scale sc = make_scale<QMAX>(am);
+    const Scale sc = lane32_block_scale<QMAX, LOGB, WPB>(acc, red, parity, warp, gid, lane);
     const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;
     const int64_t obase = ((int64_t)dn * a.G + dl) * a.R + e_warp;
-    uint32_t out[BITS];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      uint32_t c[8];
-      quantize8<QMAX>(acc[m], sc, c);
-      if constexpr (BITS == 4) {
-        out[m] = pack_i4x8(c);
-      } else {
-        const uint2 p = pack_i8x8(c);
-        out[2 * m] = p.x;
-        out[2 * m + 1] = p.y;
-      }
-    }
-    uint4* co = reinterpret_cast<uint4*>(a.codes_out + ((obase * BITS) >> 3) + lane * LCB);
-#pragma unroll
-    for (int h = 0; h < BITS / 4; ++h)
-      co[h] = make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+    lane32_quantize_store<BITS>(acc, sc, a.codes_out + ((obase * BITS) >> 3) + lane * LCB);
     // R is a multiple of B, so obase mod B = e_warp mod B
     const int eb = (int)(e_warp & (G::B - 1)) + lane_e;
     if ((eb & (G::B - 1)) == 0) a.scales_out[(obase >> LOGB) + (eb >> LOGB)] = sc.s;

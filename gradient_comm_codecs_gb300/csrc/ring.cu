@@ -160,7 +160,6 @@ __global__ void __launch_bounds__(kThreads, 2) ring1_kernel(const RingArgs a) {
   using G = Geo<LOGB, kRingRows>;
   constexpr int WPB = G::WPB, GPC = kWarps / WPB;
   constexpr int QMAX = (1 << (BITS - 1)) - 1;
-  constexpr int LB = G::B >= 1024 ? 32 : G::B / 32;  // lanes sharing a block within a warp
   constexpr int CV = BITS / 4;                       // 16-byte code vectors of a lane
   constexpr unsigned kAll = 0xffffffffu;
   __shared__ float red[2][kWarps];
@@ -216,7 +215,6 @@ __global__ void __launch_bounds__(kThreads, 2) ring1_kernel(const RingArgs a) {
     }
   };
 
-  const float2 one2 = make_float2(a.one, a.one);
   Row cur_row = row_of(r), nxt_row = cur_row;
   Loads cur, nxt;
   load(cur, cur_row, t);
@@ -242,21 +240,7 @@ __global__ void __launch_bounds__(kThreads, 2) ring1_kernel(const RingArgs a) {
     if (has_input) {  // own + D(msg), each rounded
       bool fma_path = false;
       if constexpr (BITS == 4) fma_path = __all_sync(kAll, cur.s < kI4FmaMaxScale);
-      if (fma_path) {
-        if constexpr (BITS == 4) {
-          const I4Fma k = i4_fma_scale(cur.s);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) dequant_acc_i4(cur.c[m], k, one2, v[m]);
-        }
-      } else {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          float q[8];
-          if constexpr (BITS == 4) decode8<4>(cur.c[m], q);
-          else decode8<8>(make_uint2(cur.c[2 * m], cur.c[2 * m + 1]), q);
-          accumulate8(v[m], q, cur.s, a.one);
-        }
-      }
+      lane32_dequant_acc<BITS>(cur.c, cur.s, fma_path, a.one, v);
     }
     const int64_t e = t * G::U + e_lane;  // the lane's first element within the chunk
     if constexpr (MODE == kRingLast) {
@@ -274,36 +258,8 @@ __global__ void __launch_bounds__(kThreads, 2) ring1_kernel(const RingArgs a) {
         st8_cs(go + 8 * m, WIDE, g);
       }
     } else {  // requantize the lane's 32 values with its block's scale
-      float m0 = 0.0f, m1 = 0.0f, m2 = 0.0f, m3 = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        m0 = fmaxf(m0, fabsf(v[0][i]));
-        m1 = fmaxf(m1, fabsf(v[1][i]));
-        m2 = fmaxf(m2, fabsf(v[2][i]));
-        m3 = fmaxf(m3, fabsf(v[3][i]));
-      }
-      float am = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-#pragma unroll
-      for (int o = 1; o < LB; o <<= 1) am = fmaxf(am, __shfl_xor_sync(kAll, am, o));
-      if constexpr (WPB > 1) am = group_absmax<WPB>(am, red, parity, warp, gid, lane);
-      const Scale sc = make_scale<QMAX>(am);
-      uint32_t out[BITS];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        uint32_t c[8];
-        quantize8<QMAX>(v[m], sc, c);
-        if constexpr (BITS == 4) {
-          out[m] = pack_i4x8(c);
-        } else {
-          const uint2 p = pack_i8x8(c);
-          out[2 * m] = p.x;
-          out[2 * m + 1] = p.y;
-        }
-      }
-      uint4* co = reinterpret_cast<uint4*>(a.codes_out + r * a.cb + ((e * BITS) >> 3));
-#pragma unroll
-      for (int h = 0; h < CV; ++h)
-        co[h] = make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+      const Scale sc = lane32_block_scale<QMAX, LOGB, WPB>(v, red, parity, warp, gid, lane);
+      lane32_quantize_store<BITS>(v, sc, a.codes_out + r * a.cb + ((e * BITS) >> 3));
       if ((e & (G::B - 1)) == 0) a.scales_out[r * a.nb + (e >> LOGB)] = sc.s;
     }
     r = rn;
