@@ -791,3 +791,52 @@ def test_run_from_host_successive_steps(input_sets):
     assert_f32_bitexact(np_f32(path.grad_out), gref, "third step's reduced gradient")
     assert_rel_close(np_f32(path.master), p, 1e-5, "master after three steps")
     assert_bf16_ulp(u16(p_host), pb, "parameters copied back after three steps")
+
+
+def _fuzz_cases(n, seed):
+    """Seeded random topologies, block sizes, widths and slice lengths: whole 1024-element
+    units or ragged, G a multiple of 4 or not, blocks within or across warps."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        N = int(rng.choice([1, 2, 2, 3, 4]))
+        G = int(rng.choice([1, 2, 3, 4, 4, 5, 8, 8, 12, 16]))
+        block = int(rng.choice(BLOCKS))
+        bits = int(rng.choice([4, 8]))
+        if rng.random() < 0.5:  # whole units: L a multiple of max(1024, B)
+            L = max(1024, block) * int(rng.integers(1, 4))
+        else:
+            L = block * int(rng.integers(1, 12))
+        Nd = N * G
+        if Nd * Nd * L > (1 << 23):
+            continue
+        cases.append((N, G, block, bits, L, int(rng.integers(0, 1 << 30))))
+    return cases
+
+
+@pytest.mark.parametrize("N,G,block,bits,L,seed", _fuzz_cases(48, 2024))
+def test_fuzz_qgz_chain_and_ring(N, G, block, bits, L, seed):
+    """Random shapes through every dispatch branch of the reduce: one-shot reorder+quant,
+    hop 1, hop 2 (or the single final hop) and the quantized ring, against the oracle."""
+    Z = zpp()
+    rng = np.random.default_rng(seed)
+    Nd = N * G
+    bucket = Nd * L
+    x = (rng.standard_t(3, Nd * bucket) * 1e-3).astype(np.float32)
+    xb = x.reshape(-1, block)
+    xb[rng.integers(0, xb.shape[0], size=max(1, xb.shape[0] // 50))] *= 100.0
+    gb = oracle.f32_to_bf16(x)
+    got = run_gpu_chain(Z, gb, N, G, bucket, block, bits)
+    c1, s1 = oracle.qgz_reorder_quant(gb, N, G, bucket, block, bits)
+    assert_bytes_equal(np_bytes(got["c1"]), c1, "one-shot codes")
+    assert_f32_bitexact(np_f32(got["s1"]), s1, "one-shot scales")
+    if N == 1:
+        want = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
+    else:
+        c2, s2 = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
+        assert_bytes_equal(np_bytes(got["c2"]), c2, "hop-1 codes")
+        assert_f32_bitexact(np_f32(got["s2"]), s2, "hop-1 scales")
+        want = oracle.qgz_hop2(c2, s2, N, G, bucket, block, bits)
+    assert_f32_bitexact(np_f32(got["grad"]), want, "reduced gradient")
+    _, g = run_gpu_ring(Z, gb, Nd, bucket, block, bits)
+    assert_f32_bitexact(g, oracle.ring_reduce_scatter(gb, Nd, bucket, block, bits), "ring")
