@@ -405,8 +405,9 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
 // loaded while the last chunk of this unit is summed, so the loads never
 // drain between units.  Requires S to be a multiple of 2*SCH.
 //
-// int4 chunks whose scales are all below 2^-5 (a warp vote) are dequantized
-// by one FMA a code (dequant_acc_i4); others by the magic-number decode.
+// Chunks whose scales are all below 2^-5 (a warp vote) are dequantized by one
+// FMA a code (dequant_acc_i4 / dequant_acc_i8); others by the magic-number
+// decode.
 template <int BITS, int LOGB, int SCH>
 __global__ void __launch_bounds__(kThreads, 2) hop1_kernel(const HopArgs a) {
   using G = Geo<LOGB, 4>;
@@ -456,20 +457,22 @@ __global__ void __launch_bounds__(kThreads, 2) hop1_kernel(const HopArgs a) {
   float acc[4][8];
   const float2 one2 = make_float2(a.one, a.one);
   auto sum = [&](const Chunk& ch) {
-    bool fma_path = false;
-    if constexpr (BITS == 4) {
-      float smax = ch.s[0];
+    float smax = ch.s[0];
 #pragma unroll
-      for (int j = 1; j < SCH; ++j) smax = fmaxf(smax, ch.s[j]);
-      fma_path = __all_sync(kAll, smax < kI4FmaMaxScale);
-    }
+    for (int j = 1; j < SCH; ++j) smax = fmaxf(smax, ch.s[j]);
+    const bool fma_path = __all_sync(kAll, smax < kFmaDequantMaxScale);
     if (fma_path) {
-      if constexpr (BITS == 4) {
 #pragma unroll
-        for (int j = 0; j < SCH; ++j) {
+      for (int j = 0; j < SCH; ++j) {
+        if constexpr (BITS == 4) {
           const I4Fma k = i4_fma_scale(ch.s[j]);
 #pragma unroll
           for (int m = 0; m < 4; ++m) dequant_acc_i4(ch.w[j][m], k, one2, acc[m]);
+        } else {
+          const I8Fma k = i8_fma_scale(ch.s[j]);
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            dequant_acc_i8(make_uint2(ch.w[j][2 * m], ch.w[j][2 * m + 1]), k, one2, acc[m]);
         }
       }
     } else {

@@ -152,9 +152,9 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const RingArgs a) {
 // incoming message; a block of B <= 1024 elements is B/32 neighbouring lanes.
 // The next unit's loads are in flight while the current one is computed.
 //
-// int4 units whose incoming scales are all below 2^-5 (a warp vote) are
-// dequantized by one FMA a code (dequant_acc_i4); others by the magic-number
-// decode.  WIDE: x and grad_out 32-byte aligned.
+// Units whose incoming scales are all below 2^-5 (a warp vote) are
+// dequantized by one FMA a code (dequant_acc_i4 / dequant_acc_i8); others by
+// the magic-number decode.  WIDE: x and grad_out 32-byte aligned.
 //
 // Three CTAs an SM (80 registers, a few values spilled to L1): the kernel waits
 // on memory, and the extra warps hide more of it than the spills cost
@@ -242,8 +242,7 @@ __global__ void __launch_bounds__(kThreads, 3) ring1_kernel(const RingArgs a) {
         v[m][2 * i + 1] = bf16_hi(w);
       }
     if (has_input) {  // own + D(msg), each rounded
-      bool fma_path = false;
-      if constexpr (BITS == 4) fma_path = __all_sync(kAll, cur.s < kI4FmaMaxScale);
+      const bool fma_path = __all_sync(kAll, cur.s < kFmaDequantMaxScale);
       lane32_dequant_acc<BITS>(cur.c, cur.s, fma_path, a.one, v);
     }
     const int64_t e = t * G::U + e_lane;  // the lane's first element within the chunk

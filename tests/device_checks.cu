@@ -16,14 +16,15 @@
 //  dequant_acc_i4(w, i4_fma_scale(s), 1, acc) == acc + fl(q * s), each rounded,
 //      for all 16 int4 codes q and every float s in [0, 2^-5) (exhaustive), with
 //      acc a seeded value of the scale's magnitude (the one-FMA int4 dequantization)
+//  dequant_acc_i8 likewise: all 256 int8 codes and every float s in [0, 2^-5)
 #include <cstdio>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "zpp_device.cuh"
 
-__device__ unsigned long long g_bad[7];
-__device__ unsigned int g_first[7];
+__device__ unsigned long long g_bad[8];
+__device__ unsigned int g_first[8];
 
 __global__ void check_div(uint32_t lo, uint32_t hi) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -171,8 +172,35 @@ __global__ void check_i4fma(uint32_t lo, uint32_t hi) {
   }
 }
 
+__global__ void check_i8fma(uint32_t lo, uint32_t hi) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t b = lo + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; b < hi; b += stride) {
+    const float s = __uint_as_float((uint32_t)b);
+    const zpp::I8Fma k = zpp::i8_fma_scale(s);
+    const uint32_t h = mix((uint32_t)b ^ 0x5bd1e995u);
+    const float a0 = __fmul_rn(s, (float)((int)(h >> 8) - (1 << 23)) * (1.0f / 1048576.0f));
+    const float2 one2 = make_float2(1.0f, 1.0f);
+    for (int g = 0; g < 32; ++g) {  // codes 8g .. 8g+7 as bytes, q = (int8_t)byte
+      uint32_t lo8 = 0, hi8 = 0;
+      for (int e = 0; e < 4; ++e) {
+        lo8 |= (uint32_t)(8 * g + e) << (8 * e);
+        hi8 |= (uint32_t)(8 * g + 4 + e) << (8 * e);
+      }
+      float acc[8];
+      for (int e = 0; e < 8; ++e) acc[e] = a0;
+      zpp::dequant_acc_i8(make_uint2(lo8, hi8), k, one2, acc);
+      for (int e = 0; e < 8; ++e) {
+        const int q = (int)(int8_t)(uint8_t)(8 * g + e);
+        if (acc[e] != __fadd_rn(a0, __fmul_rn((float)q, s))) {
+          if (atomicAdd(&g_bad[7], 1ull) == 0) g_first[7] = (uint32_t)b;
+        }
+      }
+    }
+  }
+}
+
 int main() {
-  unsigned long long zero[7] = {0, 0, 0, 0, 0, 0, 0};
+  unsigned long long zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (cudaMemcpyToSymbol(g_bad, zero, sizeof zero) != cudaSuccess) return 2;
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
@@ -181,9 +209,10 @@ int main() {
   check_rcp<<<sms * 8, 256>>>(0x2B800000u, 0x3F800000u);  // 2^-40 .. 1
   check_bcdiv<<<sms * 8, 256>>>(1ull << 32);
   check_i4fma<<<sms * 8, 256>>>(0u, 0x3D000000u);  // +0 .. just below 2^-5
+  check_i8fma<<<sms * 8, 256>>>(0u, 0x3D000000u);
   if (cudaDeviceSynchronize() != cudaSuccess) return 3;
-  unsigned long long bad[7];
-  unsigned int first[7];
+  unsigned long long bad[8];
+  unsigned int first[8];
   cudaMemcpyFromSymbol(bad, g_bad, sizeof bad);
   cudaMemcpyFromSymbol(first, g_first, sizeof first);
   printf("div_qmax7 %llu %08x\n", bad[0], bad[0] ? first[0] : 0u);
@@ -193,5 +222,6 @@ int main() {
   printf("bias_rcp %llu %08x\n", bad[4], bad[4] ? first[4] : 0u);
   printf("bias_div %llu %08x\n", bad[5], bad[5] ? first[5] : 0u);
   printf("i4_fma %llu %08x\n", bad[6], bad[6] ? first[6] : 0u);
+  printf("i8_fma %llu %08x\n", bad[7], bad[7] ? first[7] : 0u);
   return 0;
 }

@@ -7,7 +7,8 @@ quotient on 2^33 seeded draws of 8 values per bit width, most of them within
 division equal the IEEE ones (exhaustive over the divisors, 2^32 seeded
 dividend pairs); and the one-FMA int4 dequantize-and-add, a subnormal code
 times the scale scaled by 2^133, equals the product and sum rounded one after
-the other for every code and every scale below 2^-5 (exhaustive)."""
+the other for every code and every scale below 2^-5 (exhaustive), for int4
+and for int8."""
 import os
 import subprocess
 
@@ -30,4 +31,4 @@ def test_exhaustive_device_identities(tmp_path):
     assert out.returncode == 0, out.stdout + out.stderr
     res = {line.split()[0]: int(line.split()[1]) for line in out.stdout.splitlines()}
     assert res == {"div_qmax7": 0, "div_qmax127": 0, "quantize_q7": 0, "quantize_q127": 0,
-                   "bias_rcp": 0, "bias_div": 0, "i4_fma": 0}, out.stdout
+                   "bias_rcp": 0, "bias_div": 0, "i4_fma": 0, "i8_fma": 0}, out.stdout
