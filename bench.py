@@ -8,9 +8,12 @@ with every simulated rank's buffers resident in HBM:
     receiver) -> qgZ reorder + one-shot quant (all ranks' buckets) -> hop 1
     [-> hop 2] -> x 1/N_d fused into the sharded Adam step.
 
-Default workload: the llama-layer bucket (Phi = 202,375,168 bf16 parameters,
-N_d = 8 simulated as 1 node x 8 GPUs, qwZ int8 B=512, qgZ int4 B=512, Adam on
-all 8 owned shards).  `value` is algorithmic bytes moved per step (the bytes
+Default workload: the 7B model, the largest configuration (qwZ int8 B=2048
+over 7e9 bf16 weights in 27 calls of up to 2^28 elements; qgZ over N_d = 64
+simulated as 8 nodes x 8 GPUs with a 2^26-element int4 B=256 bucket per rank
+and the Adam step fused on the final hop; standalone Adam over the rest of
+the 109,375,000-parameter owned shard).  `--config llama` is the llama-layer
+bucket (Phi = 202,375,168, N_d = 8 as 1 node x 8 GPUs, int8/int4 B=512).  `value` is algorithmic bytes moved per step (the bytes
 each kernel must read and write, summed over the pass) divided by the step
 time, in GB/s; `qgz_bucket_elems_per_s` is N_d * bucket / (qgZ kernels' time).
 
@@ -588,6 +591,33 @@ class OracleSample:
             oracle.adam_step(g, p, z, z, a.lr, a.beta1, a.beta2, a.eps, a.step)
 
 
+def host_cpu():
+    """CPU model and online core count of this host."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip().lower() in ("model name", "cpu model"):
+                    model = v.strip()
+                    break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                k, _, v = line.partition(":")
+                if k.strip() == "Model name":
+                    model = v.strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    import platform
+    return {"cpu_model": model or platform.processor() or platform.machine(),
+            "nproc": os.cpu_count()}
+
+
 def sized_sample(wl, seconds, microbatches=1, hpz=False, ring=False):
     """Calibrate the sample so one oracle pass takes about `seconds`."""
     s = OracleSample(wl, 4, 2, microbatches, hpz, ring)
@@ -609,6 +639,7 @@ def cpu_baseline(wl, seconds=12.0, microbatches=1, hpz=False, ring=False):
             break
     dt = (time.perf_counter() - t) / n
     return {"value": s.steps_bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            **host_cpu(),
             "sample": f"{s.steps_bytes / 1e6:.1f} MB of algorithmic traffic per pass: the first "
                       f"blocks of every shard and of every slice of every rank (same topology, "
                       f"block, bits, Adam), {n} passes, single-threaded C oracle",
@@ -635,6 +666,7 @@ def run_reference(args, wl):
         "config": workload_config(wl, args.config, microbatches=args.microbatches, hpz=args.hpz,
                                   ring=args.ring),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         **host_cpu(),
                          "sample": f"{s.steps_bytes / 1e6:.1f} MB of algorithmic traffic per "
                                    "step: the first blocks of every shard and slice of every "
                                    "rank, single-threaded C oracle"},
@@ -801,7 +833,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="llama", choices=["tiny", "llama", "two_hop", "7b"])
+    ap.add_argument("--config", default="7b", choices=["tiny", "llama", "two_hop", "7b"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fuse-qwz", action="store_true",
                     help="produce the weights' qwZ message inside the final hop's Adam pass")

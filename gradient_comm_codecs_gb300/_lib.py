@@ -4,13 +4,20 @@ of the path runs in the CUDA kernels behind these calls.
 
 Tensors are passed as torch tensors on a CUDA device (contiguous, of the dtype
 the header states) and turned into raw device pointers; `stream` defaults to
-torch's current stream on the tensors' device.  A nonzero status raises
-``ZppError``.  If the library has not been built the first call raises: there
-is no fallback path.
+torch's current stream on the tensors' device, and the call runs with that
+device current.  Before the C call every tensor argument is checked against
+the bytes the call will read or write (computed from the scalar arguments by
+the header's size rules) and against the other tensors' device: a tensor that
+is too small, or on another device, raises ValueError and nothing is
+launched.  (Raw integer pointers are passed through unchecked.)  A nonzero
+status raises ``ZppError``.  If the library has not been built the first call
+raises: there is no fallback path.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
+import numbers
 import os
 
 import torch
@@ -131,43 +138,124 @@ def _check(status, where):
         raise ZppError(status, where)
 
 
+# ---- size and device checks (before anything is launched) ----------------------------
+
+def _cb(n, bits):
+    """Code bytes of n elements (the header's zpp_codes_bytes rule)."""
+    return (n * bits + 7) // 8
+
+
+def _nb(n, block):
+    """Blocks of n elements (the header's zpp_num_blocks rule)."""
+    return -(-n // block)
+
+
+def _guard(where, *needs):
+    """Check every (tensor, bytes needed, name) of a call and return a context
+    that makes the tensors' device current.  Sizes are only checked when the
+    scalar arguments are well formed; malformed ones are left for the
+    library's own validation (it returns ZPP_ERR_INVALID_ARG)."""
+    dev = None
+    for t, need, name in needs:
+        if not isinstance(t, torch.Tensor):
+            continue
+        if t.is_cuda:
+            if dev is None:
+                dev = t.device
+            elif t.device != dev:
+                raise ValueError(f"{where}: {name} is on {t.device}, other arguments on {dev}")
+        if need is not None and need > 0:
+            have = t.numel() * t.element_size()
+            if have < need:
+                raise ValueError(f"{where}: {name} is too small: {have} bytes, the call "
+                                 f"accesses {need}")
+    return torch.cuda.device(dev) if dev is not None else contextlib.nullcontext()
+
+
+def _ok(*vals):
+    """True when every size argument is a non-negative int and every block /
+    bit width is usable for the size rules."""
+    return all(isinstance(v, numbers.Integral) and v >= 0 for v in vals)
+
+
+def _codec_ok(block, bits):
+    return _ok(block, bits) and block > 0 and bits in (4, 8, 16)
+
+
 # ---- entry points ---------------------------------------------------------------------
 
 def zpp_qwz_quant(x_bf16, nranks, shard_elems, block, bits, codes, scales, stream=None):
-    _check(_lib().zpp_qwz_quant(_dev(x_bf16, _BF16, "x_bf16"), nranks, shard_elems, block, bits,
-                                _dev(codes, _BYTES, "codes"), _dev(scales, _F32, "scales"),
-                                _stream(stream, x_bf16)), "zpp_qwz_quant")
+    ok = _ok(nranks, shard_elems) and _codec_ok(block, bits)
+    n = nranks * shard_elems if ok else None
+    with _guard("zpp_qwz_quant", (x_bf16, ok and 2 * n, "x_bf16"),
+                (codes, ok and nranks * _cb(shard_elems, bits), "codes"),
+                (scales, ok and 4 * nranks * _nb(shard_elems, block), "scales")):
+        _check(_lib().zpp_qwz_quant(_dev(x_bf16, _BF16, "x_bf16"), nranks, shard_elems, block,
+                                    bits, _dev(codes, _BYTES, "codes"),
+                                    _dev(scales, _F32, "scales"), _stream(stream, x_bf16)),
+               "zpp_qwz_quant")
 
 
 def zpp_qwz_dequant(codes, scales, nranks, shard_elems, block, bits, y_bf16, stream=None):
-    _check(_lib().zpp_qwz_dequant(_dev(codes, _BYTES, "codes"), _dev(scales, _F32, "scales"),
-                                  nranks, shard_elems, block, bits, _dev(y_bf16, _BF16, "y_bf16"),
-                                  _stream(stream, codes)), "zpp_qwz_dequant")
+    ok = _ok(nranks, shard_elems) and _codec_ok(block, bits)
+    with _guard("zpp_qwz_dequant", (codes, ok and nranks * _cb(shard_elems, bits), "codes"),
+                (scales, ok and 4 * nranks * _nb(shard_elems, block), "scales"),
+                (y_bf16, ok and 2 * nranks * shard_elems, "y_bf16")):
+        _check(_lib().zpp_qwz_dequant(_dev(codes, _BYTES, "codes"), _dev(scales, _F32, "scales"),
+                                      nranks, shard_elems, block, bits,
+                                      _dev(y_bf16, _BF16, "y_bf16"), _stream(stream, codes)),
+               "zpp_qwz_dequant")
+
+
+def _qgz_msg(nodes, gpus_per_node, bucket_elems, block, bits):
+    """(ranks, one-shot code bytes, one-shot scale bytes) of a qgZ bucket, or
+    None when the arguments are malformed."""
+    if not (_ok(nodes, gpus_per_node, bucket_elems) and _codec_ok(block, bits)):
+        return None
+    nd = nodes * gpus_per_node
+    if nd < 1:
+        return None
+    return nd, nd * _cb(bucket_elems, bits), 4 * nd * (bucket_elems // block)
 
 
 def zpp_qgz_reorder_quant(grads_bf16, nodes, gpus_per_node, bucket_elems, block, bits, codes,
                           scales, stream=None):
-    _check(_lib().zpp_qgz_reorder_quant(_dev(grads_bf16, _BF16, "grads_bf16"), nodes,
-                                        gpus_per_node, bucket_elems, block, bits,
-                                        _dev(codes, _BYTES, "codes"), _dev(scales, _F32, "scales"),
-                                        _stream(stream, grads_bf16)), "zpp_qgz_reorder_quant")
+    m = _qgz_msg(nodes, gpus_per_node, bucket_elems, block, bits)
+    with _guard("zpp_qgz_reorder_quant",
+                (grads_bf16, m and 2 * m[0] * bucket_elems, "grads_bf16"),
+                (codes, m and m[1], "codes"), (scales, m and m[2], "scales")):
+        _check(_lib().zpp_qgz_reorder_quant(_dev(grads_bf16, _BF16, "grads_bf16"), nodes,
+                                            gpus_per_node, bucket_elems, block, bits,
+                                            _dev(codes, _BYTES, "codes"),
+                                            _dev(scales, _F32, "scales"),
+                                            _stream(stream, grads_bf16)),
+               "zpp_qgz_reorder_quant")
 
 
 def zpp_grad_accumulate(grads_bf16, acc, n, first, stream=None):
-    _check(_lib().zpp_grad_accumulate(_dev(grads_bf16, _BF16, "grads_bf16"), _dev(acc, _F32, "acc"),
-                                      n, int(first), _stream(stream, grads_bf16)),
-           "zpp_grad_accumulate")
+    ok = _ok(n)
+    with _guard("zpp_grad_accumulate", (grads_bf16, ok and 2 * n, "grads_bf16"),
+                (acc, ok and 4 * n, "acc")):
+        _check(_lib().zpp_grad_accumulate(_dev(grads_bf16, _BF16, "grads_bf16"),
+                                          _dev(acc, _F32, "acc"), n, int(first),
+                                          _stream(stream, grads_bf16)),
+               "zpp_grad_accumulate")
 
 
 def zpp_qgz_reorder_quant_acc(grads_bf16, acc, nodes, gpus_per_node, bucket_elems, block, bits,
                               codes, scales, stream=None):
-    _check(_lib().zpp_qgz_reorder_quant_acc(_dev(grads_bf16, _BF16, "grads_bf16"),
-                                            _dev(acc, _F32, "acc"), nodes, gpus_per_node,
-                                            bucket_elems, block, bits,
-                                            _dev(codes, _BYTES, "codes"),
-                                            _dev(scales, _F32, "scales"),
-                                            _stream(stream, grads_bf16)),
-           "zpp_qgz_reorder_quant_acc")
+    m = _qgz_msg(nodes, gpus_per_node, bucket_elems, block, bits)
+    with _guard("zpp_qgz_reorder_quant_acc",
+                (grads_bf16, m and 2 * m[0] * bucket_elems, "grads_bf16"),
+                (acc, m and 4 * m[0] * bucket_elems, "acc"),
+                (codes, m and m[1], "codes"), (scales, m and m[2], "scales")):
+        _check(_lib().zpp_qgz_reorder_quant_acc(_dev(grads_bf16, _BF16, "grads_bf16"),
+                                                _dev(acc, _F32, "acc"), nodes, gpus_per_node,
+                                                bucket_elems, block, bits,
+                                                _dev(codes, _BYTES, "codes"),
+                                                _dev(scales, _F32, "scales"),
+                                                _stream(stream, grads_bf16)),
+               "zpp_qgz_reorder_quant_acc")
 
 
 def _adam_args(adam, state):
@@ -185,42 +273,87 @@ def _adam_args(adam, state):
             ctypes.byref(st) if st is not None else None, hp, st)
 
 
+def _state_needs(state, n):
+    """(tensor, bytes, name) of an Adam state tuple over n parameters."""
+    if not isinstance(state, (tuple, list)):
+        return []
+    master, m, v, param = state
+    ok = n is not None
+    return [(master, ok and 4 * n, "master"), (m, ok and 4 * n, "m"), (v, ok and 4 * n, "v"),
+            (param, ok and 2 * n, "param_bf16")]
+
+
+def _hop_needs(hop, nodes, gpus_per_node, bucket_elems, block, bits, codes_in, scales_in,
+               codes_out, scales_out, grad_out, state):
+    m = _qgz_msg(nodes, gpus_per_node, bucket_elems, block, bits)
+    needs = []
+    if m is None or hop not in (1, 2):
+        return [(codes_in, None, "codes_in"), (scales_in, None, "scales_in"),
+                (codes_out, None, "codes_out"), (scales_out, None, "scales_out"),
+                (grad_out, None, "grad_out")] + _state_needs(state, None)
+    nd = m[0]
+    L = bucket_elems // nd
+    two = (nd * _cb(nodes * L, bits), 4 * nd * (nodes * L // block))  # hop-1 message
+    cin, sin = (m[1], m[2]) if hop == 1 else two
+    needs += [(codes_in, cin, "codes_in"), (scales_in, sin, "scales_in"),
+              (codes_out, two[0], "codes_out"), (scales_out, two[1], "scales_out"),
+              (grad_out, 4 * bucket_elems, "grad_out")]
+    return needs + _state_needs(state, bucket_elems)
+
+
 def zpp_qgz_hop_reduce(hop, codes_in, scales_in, nodes, gpus_per_node, bucket_elems, block, bits,
                        codes_out=None, scales_out=None, grad_out=None, adam=None, state=None,
                        stream=None):
     """`adam`: (lr, beta1, beta2, eps, step) or zpp_adam_hparams; `state`:
     (master, m, v, param_bf16_or_None) tensors or zpp_adam_state."""
-    hp, st, _keep1, _keep2 = _adam_args(adam, state)
-    _check(_lib().zpp_qgz_hop_reduce(hop, _dev(codes_in, _BYTES, "codes_in"),
-                                     _dev(scales_in, _F32, "scales_in"), nodes, gpus_per_node,
-                                     bucket_elems, block, bits,
-                                     _dev(codes_out, _BYTES, "codes_out"),
-                                     _dev(scales_out, _F32, "scales_out"),
-                                     _dev(grad_out, _F32, "grad_out"), hp, st,
-                                     _stream(stream, codes_in)), "zpp_qgz_hop_reduce")
+    needs = _hop_needs(hop, nodes, gpus_per_node, bucket_elems, block, bits, codes_in, scales_in,
+                       codes_out, scales_out, grad_out, state)
+    with _guard("zpp_qgz_hop_reduce", *needs):
+        hp, st, _keep1, _keep2 = _adam_args(adam, state)
+        _check(_lib().zpp_qgz_hop_reduce(hop, _dev(codes_in, _BYTES, "codes_in"),
+                                         _dev(scales_in, _F32, "scales_in"), nodes, gpus_per_node,
+                                         bucket_elems, block, bits,
+                                         _dev(codes_out, _BYTES, "codes_out"),
+                                         _dev(scales_out, _F32, "scales_out"),
+                                         _dev(grad_out, _F32, "grad_out"), hp, st,
+                                         _stream(stream, codes_in)), "zpp_qgz_hop_reduce")
 
 
 def zpp_qgz_final_hop_adam_qwz(hop, codes_in, scales_in, nodes, gpus_per_node, bucket_elems,
                                block, bits, grad_out, adam, state, qwz_bits, qwz_codes,
                                qwz_scales, stream=None):
-    hp, st, _keep1, _keep2 = _adam_args(adam, state)
-    _check(_lib().zpp_qgz_final_hop_adam_qwz(
-        hop, _dev(codes_in, _BYTES, "codes_in"), _dev(scales_in, _F32, "scales_in"), nodes,
-        gpus_per_node, bucket_elems, block, bits, _dev(grad_out, _F32, "grad_out"), hp, st,
-        qwz_bits, _dev(qwz_codes, _BYTES, "qwz_codes"), _dev(qwz_scales, _F32, "qwz_scales"),
-        _stream(stream, codes_in)), "zpp_qgz_final_hop_adam_qwz")
+    needs = _hop_needs(hop, nodes, gpus_per_node, bucket_elems, block, bits, codes_in, scales_in,
+                       None, None, grad_out, state)
+    ok = _ok(bucket_elems) and _codec_ok(block, bits)
+    needs += [(qwz_codes, ok and bucket_elems, "qwz_codes"),
+              (qwz_scales, ok and 4 * (bucket_elems // block), "qwz_scales")]
+    with _guard("zpp_qgz_final_hop_adam_qwz", *needs):
+        hp, st, _keep1, _keep2 = _adam_args(adam, state)
+        _check(_lib().zpp_qgz_final_hop_adam_qwz(
+            hop, _dev(codes_in, _BYTES, "codes_in"), _dev(scales_in, _F32, "scales_in"), nodes,
+            gpus_per_node, bucket_elems, block, bits, _dev(grad_out, _F32, "grad_out"), hp, st,
+            qwz_bits, _dev(qwz_codes, _BYTES, "qwz_codes"), _dev(qwz_scales, _F32, "qwz_scales"),
+            _stream(stream, codes_in)), "zpp_qgz_final_hop_adam_qwz")
 
 
 def zpp_ring_rs_step(step, nranks, bucket_elems, block, bits, grads_bf16, codes_in=None,
                      scales_in=None, codes_out=None, scales_out=None, grad_out=None, stream=None):
-    _check(_lib().zpp_ring_rs_step(step, nranks, bucket_elems, block, bits,
-                                   _dev(grads_bf16, _BF16, "grads_bf16"),
-                                   _dev(codes_in, _BYTES, "codes_in"),
-                                   _dev(scales_in, _F32, "scales_in"),
-                                   _dev(codes_out, _BYTES, "codes_out"),
-                                   _dev(scales_out, _F32, "scales_out"),
-                                   _dev(grad_out, _F32, "grad_out"), _stream(stream, grads_bf16)),
-           "zpp_ring_rs_step")
+    ok = _ok(nranks, bucket_elems) and nranks > 0 and _codec_ok(block, bits)
+    L = bucket_elems // nranks if ok else 0
+    cb, sb = (nranks * _cb(L, bits), 4 * nranks * (L // block)) if ok else (None, None)
+    with _guard("zpp_ring_rs_step", (grads_bf16, ok and 2 * nranks * bucket_elems, "grads_bf16"),
+                (codes_in, cb, "codes_in"), (scales_in, sb, "scales_in"),
+                (codes_out, cb, "codes_out"), (scales_out, sb, "scales_out"),
+                (grad_out, ok and 4 * bucket_elems, "grad_out")):
+        _check(_lib().zpp_ring_rs_step(step, nranks, bucket_elems, block, bits,
+                                       _dev(grads_bf16, _BF16, "grads_bf16"),
+                                       _dev(codes_in, _BYTES, "codes_in"),
+                                       _dev(scales_in, _F32, "scales_in"),
+                                       _dev(codes_out, _BYTES, "codes_out"),
+                                       _dev(scales_out, _F32, "scales_out"),
+                                       _dev(grad_out, _F32, "grad_out"),
+                                       _stream(stream, grads_bf16)),
+               "zpp_ring_rs_step")
 
 
 def zpp_hpz_gather(gpus_per_node, shards_per_rank, shard_elems, block, bits, sec_codes,
@@ -230,18 +363,27 @@ def zpp_hpz_gather(gpus_per_node, shards_per_rank, shard_elems, block, bits, sec
     G = len(sec_codes)
     if G != gpus_per_node:
         raise ValueError("one secondary partition per local rank")
-    cp = (ctypes.c_void_p * G)(*[_dev(t, _BF16 if bits == 16 else _BYTES, "sec_codes")
-                                 for t in sec_codes])
-    sp = None
+    ok = _ok(shards_per_rank, shard_elems) and _codec_ok(block, bits)
+    N = shards_per_rank
+    cbytes = (N * (2 * shard_elems if bits == 16 else _cb(shard_elems, bits))) if ok else None
+    needs = [(t, cbytes, f"sec_codes[{l}]") for l, t in enumerate(sec_codes)]
     if bits != 16:
         if sec_scales is None or len(sec_scales) != G:
             raise ValueError("one scale tensor per local rank")
-        sp = (ctypes.c_void_p * G)(*[_dev(t, _F32, "sec_scales") for t in sec_scales])
-    _check(_lib().zpp_hpz_gather(gpus_per_node, shards_per_rank, shard_elems, block, bits,
-                                 ctypes.cast(cp, ctypes.c_void_p),
-                                 None if sp is None else ctypes.cast(sp, ctypes.c_void_p),
-                                 _dev(y_bf16, _BF16, "y_bf16"), _stream(stream, y_bf16)),
-           "zpp_hpz_gather")
+        needs += [(t, ok and 4 * N * _nb(shard_elems, block), f"sec_scales[{l}]")
+                  for l, t in enumerate(sec_scales)]
+    needs.append((y_bf16, ok and 2 * G * N * shard_elems, "y_bf16"))
+    with _guard("zpp_hpz_gather", *needs):
+        cp = (ctypes.c_void_p * G)(*[_dev(t, _BF16 if bits == 16 else _BYTES, "sec_codes")
+                                     for t in sec_codes])
+        sp = None
+        if bits != 16:
+            sp = (ctypes.c_void_p * G)(*[_dev(t, _F32, "sec_scales") for t in sec_scales])
+        _check(_lib().zpp_hpz_gather(gpus_per_node, shards_per_rank, shard_elems, block, bits,
+                                     ctypes.cast(cp, ctypes.c_void_p),
+                                     None if sp is None else ctypes.cast(sp, ctypes.c_void_p),
+                                     _dev(y_bf16, _BF16, "y_bf16"), _stream(stream, y_bf16)),
+               "zpp_hpz_gather")
 
 
 def zpp_hpz_secondary_bytes(shards_per_rank, shard_elems, block, bits):
@@ -249,9 +391,13 @@ def zpp_hpz_secondary_bytes(shards_per_rank, shard_elems, block, bits):
 
 
 def zpp_shard_adam_step(grad, n, adam, state, stream=None):
-    hp, st, _keep1, _keep2 = _adam_args(adam, state)
-    _check(_lib().zpp_shard_adam_step(_dev(grad, _F32, "grad"), n, hp, st, _stream(stream, grad)),
-           "zpp_shard_adam_step")
+    ok = _ok(n)
+    with _guard("zpp_shard_adam_step", (grad, ok and 4 * n, "grad"),
+                *_state_needs(state, n if ok else None)):
+        hp, st, _keep1, _keep2 = _adam_args(adam, state)
+        _check(_lib().zpp_shard_adam_step(_dev(grad, _F32, "grad"), n, hp, st,
+                                          _stream(stream, grad)),
+               "zpp_shard_adam_step")
 
 
 def zpp_codes_bytes(n, bits):

@@ -392,8 +392,7 @@ cudaError_t run_quant(const QuantArgs& a0, int block, cudaStream_t st) {
     if (a.row_len % G::U == 0) {  // tiled: every unit full, 16-byte aligned
       constexpr size_t smem = q_smem<ACC>();
       const void* k = reinterpret_cast<const void*>(&quant_tiled_kernel<BITS, REORDER, LOGB, ACC>);
-      static const cudaError_t attr =
-          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      const cudaError_t attr = smem_opt_in(k, smem);
       if (attr != cudaSuccess) return attr;
       quant_tiled_kernel<BITS, REORDER, LOGB, ACC><<<grid_for(k, ctas, smem), kThreads, smem, st>>>(a);
     } else {

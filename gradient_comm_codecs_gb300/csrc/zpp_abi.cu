@@ -108,6 +108,27 @@ int grid_for(const void* kernel, int64_t work_ctas, size_t smem) {
   return g < 1 ? 1 : (int)g;
 }
 
+cudaError_t smem_opt_in(const void* kernel, size_t smem) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, size_t> done;  // (kernel, device) -> bytes opted in
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t key = reinterpret_cast<uintptr_t>(kernel) * 131u + (uint64_t)dev;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= smem) return cudaSuccess;
+  }
+  const cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+  if (r == cudaSuccess) {
+    std::lock_guard<std::mutex> lock(mu);
+    done[key] = smem;
+  }
+  return r;
+}
+
 }  // namespace zpp
 
 using namespace zpp;

@@ -72,4 +72,9 @@ cudaError_t launch_adam(const float* grad, int64_t n, const AdamConstsHost& ac, 
 // Grid size for a kernel: min(work CTAs, SMs * resident CTAs per SM).
 int grid_for(const void* kernel, int64_t work_ctas, size_t smem = 0);
 
+// Raises the kernel's dynamic shared-memory limit to `smem` bytes on the
+// current device, once per (kernel, device); a failure is returned and not
+// remembered, so a later call tries again.
+cudaError_t smem_opt_in(const void* kernel, size_t smem);
+
 }  // namespace zpp

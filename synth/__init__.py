@@ -27,18 +27,29 @@ Generator
   hash of its global block index; in a picked block one element, also chosen
   by hash, is multiplied by ``outlier_factor`` in fp32 and rounded back to
   bf16 (round to nearest even).
+
+Two implementations of the same function: the tensor path below (any torch
+device; what the GPU tests and the bench fill device buffers with) and, on the
+host, ``_gen.c`` (plain C, 32-bit unsigned arithmetic, built with gcc on first
+use), which the CPU calls of ``fill``/``at`` and ``fill_u16``/``at_u16`` use
+when it builds.  The CPU test suite checks that the two agree bit for bit.
 """
 from __future__ import annotations
 
 from dataclasses import dataclass
 from functools import lru_cache
 
+import ctypes
+import os
+import subprocess
+import threading
+
 import numpy as np
 import torch
 
 __all__ = [
     "Dist", "Recipe", "WEIGHTS", "MOMENT_M", "MOMENT_V", "SHARD_GRAD", "grad_stream",
-    "fill", "at", "hash32_int", "bf16_to_u16", "u16_to_bf16",
+    "fill", "at", "fill_u16", "at_u16", "hash32_int", "bf16_to_u16", "u16_to_bf16", "build",
 ]
 
 _M32 = 0xFFFFFFFF
@@ -176,6 +187,16 @@ def _values_at(recipe: Recipe, seed: int, stream: int, idx: torch.Tensor) -> tor
     return out
 
 
+def _fill_torch(recipe: Recipe, seed: int, stream: int, start: int, count: int,
+                out: torch.Tensor, chunk: int) -> torch.Tensor:
+    for c0 in range(0, count, chunk):
+        c1 = min(count, c0 + chunk)
+        idx = torch.arange(start + c0, start + c1, dtype=torch.int64, device=out.device)
+        out[c0:c1] = _values_at(recipe, seed, stream, idx)
+        del idx
+    return out
+
+
 def fill(recipe: Recipe, seed: int, stream: int, start: int, count: int,
          device="cpu", out: torch.Tensor | None = None, chunk: int = 1 << 25) -> torch.Tensor:
     """bf16 values of global indices [start, start+count) of ``stream``."""
@@ -183,19 +204,120 @@ def fill(recipe: Recipe, seed: int, stream: int, start: int, count: int,
     if out is None:
         out = torch.empty(count, dtype=torch.bfloat16, device=device)
     assert out.numel() == count and out.dtype == torch.bfloat16
-    for c0 in range(0, count, chunk):
-        c1 = min(count, c0 + chunk)
-        idx = torch.arange(start + c0, start + c1, dtype=torch.int64, device=device)
-        out[c0:c1] = _values_at(recipe, seed, stream, idx)
-        del idx
-    return out
+    if device.type == "cpu" and out.is_contiguous() and _host_lib() is not None:
+        fill_u16(recipe, seed, stream, start, count, out=out.view(torch.int16).numpy().view(np.uint16))
+        return out
+    return _fill_torch(recipe, seed, stream, start, count, out, chunk)
 
 
 def at(recipe: Recipe, seed: int, stream: int, idx) -> torch.Tensor:
     """bf16 values at arbitrary global indices (CPU unless idx is on a device)."""
     if not isinstance(idx, torch.Tensor):
+        if _host_lib() is not None:
+            return u16_to_bf16(at_u16(recipe, seed, stream, idx))
         idx = torch.as_tensor(np.asarray(idx, dtype=np.int64))
     return _values_at(recipe, seed, stream, idx.to(torch.int64).reshape(-1).clone())
+
+
+# ---- host fast path (_gen.c) ---------------------------------------------------------
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "_gen.c")
+_SO = os.path.join(_HERE, "libsynth.so")
+_build_lock = threading.Lock()
+_lib = None
+_lib_failed = False
+
+
+class _Outliers(ctypes.Structure):
+    _fields_ = [("block", ctypes.c_int64), ("thr", ctypes.c_uint64), ("p1", ctypes.c_uint32),
+                ("p2", ctypes.c_uint32), ("e1", ctypes.c_uint32), ("e2", ctypes.c_uint32),
+                ("factor", ctypes.c_float)]
+
+
+def build(force: bool = False) -> str:
+    """Compile the host generator with gcc, in-tree next to its source."""
+    with _build_lock:
+        if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+            tmp = _SO + f".{os.getpid()}.tmp"
+            subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-Wall",
+                                   _SRC, "-o", tmp])
+            os.replace(tmp, _SO)
+    return _SO
+
+
+def _host_lib():
+    """The compiled host generator, or None when gcc is unavailable (the
+    tensor path then serves the host too)."""
+    global _lib, _lib_failed
+    if _lib is not None or _lib_failed:
+        return _lib
+    try:
+        build()
+        try:
+            lib = ctypes.CDLL(_SO)
+        except OSError:  # e.g. a binary built for another machine
+            build(force=True)
+            lib = ctypes.CDLL(_SO)
+    except (OSError, subprocess.CalledProcessError):
+        _lib_failed = True
+        return None
+    P, I64, I32, U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+    for name in ("synth_fill", "synth_at"):
+        fn = getattr(lib, name)
+        fn.restype = None
+    lib.synth_fill.argtypes = [P, P, I32, U32, U32, I64, I64, ctypes.POINTER(_Outliers)]
+    lib.synth_at.argtypes = [P, P, I32, U32, U32, P, I64, ctypes.POINTER(_Outliers)]
+    _lib = lib
+    return lib
+
+
+@lru_cache(maxsize=None)
+def _table_u16(dist: Dist) -> np.ndarray:
+    return np.ascontiguousarray(bf16_to_u16(_table_cpu(dist)))
+
+
+def _outliers(recipe: Recipe, seed: int, stream: int):
+    if not recipe.outlier_block:
+        return None
+    p1, p2 = _keys(seed, stream ^ _OUTLIER_SALT)
+    e1, e2 = _keys(seed, stream ^ (_OUTLIER_SALT + 1))
+    return _Outliers(int(recipe.outlier_block), int(recipe.outlier_prob * 4294967296.0),
+                     p1, p2, e1, e2, float(recipe.outlier_factor))
+
+
+def fill_u16(recipe: Recipe, seed: int, stream: int, start: int, count: int,
+             out: np.ndarray | None = None) -> np.ndarray:
+    """Host bf16 bit patterns (uint16) of global indices [start, start+count)."""
+    lib = _host_lib()
+    if out is None:
+        out = np.empty(int(count), np.uint16)
+    assert out.dtype == np.uint16 and out.size == count and out.flags.c_contiguous
+    if lib is None:
+        out[:] = bf16_to_u16(_fill_torch(recipe, seed, stream, start, count,
+                                         torch.empty(count, dtype=torch.bfloat16), 1 << 22))
+        return out
+    k1, k2 = _keys(seed, stream)
+    o = _outliers(recipe, seed, stream)
+    tab = _table_u16(recipe.dist)
+    lib.synth_fill(out.ctypes.data, tab.ctypes.data, 32 - TABLE_BITS, k1, k2, int(start),
+                   int(count), ctypes.byref(o) if o is not None else None)
+    return out
+
+
+def at_u16(recipe: Recipe, seed: int, stream: int, idx) -> np.ndarray:
+    """Host bf16 bit patterns (uint16) at arbitrary global indices."""
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64).reshape(-1))
+    lib = _host_lib()
+    if lib is None:
+        return bf16_to_u16(_values_at(recipe, seed, stream, torch.from_numpy(idx.copy())))
+    out = np.empty(idx.size, np.uint16)
+    k1, k2 = _keys(seed, stream)
+    o = _outliers(recipe, seed, stream)
+    tab = _table_u16(recipe.dist)
+    lib.synth_at(out.ctypes.data, tab.ctypes.data, 32 - TABLE_BITS, k1, k2, idx.ctypes.data,
+                 idx.size, ctypes.byref(o) if o is not None else None)
+    return out
 
 
 def bf16_to_u16(t: torch.Tensor) -> np.ndarray:

@@ -212,3 +212,76 @@ def test_next_rows_validation(lib):
     assert q(3, 4, bb, 64, 8, P(A), P(A), P(A), None, None, None, None) == 1    # last: gradient
     assert q(3, 4, bb, 64, 8, P(A), P(A), P(A), None, None, P(M), None) == 2
     assert q(0, 4, 0, 64, 8, None, None, None, None, None, None, None) == 0
+
+
+# ---- the binding's size checks (no GPU: they run before any pointer is taken) ----------
+
+def _small_cases():
+    import torch
+    u16 = lambda n: torch.empty(n, dtype=torch.bfloat16)
+    u8 = lambda n: torch.empty(n, dtype=torch.uint8)
+    f32 = lambda n: torch.empty(n, dtype=torch.float32)
+    import gradient_comm_codecs_gb300 as Z
+    n, B = 4 * 1024, 256
+    nd, L = 4, 1024                       # 2 nodes x 2, bucket 4096
+    cb1, nb1 = nd * (4096 * 4) // 8, nd * 4096 // B
+    cb2, nb2 = nd * (2 * L * 4) // 8, nd * 2 * L // B
+    st = lambda k=0: (f32(4096 - k), f32(4096), f32(4096), u16(4096))
+    return [
+        ("x_bf16", lambda: Z.zpp_qwz_quant(u16(2 * n - 1), 2, n, B, 8, u8(2 * n), f32(2 * n // B))),
+        ("codes", lambda: Z.zpp_qwz_quant(u16(2 * n), 2, n, B, 8, u8(2 * n - 1), f32(2 * n // B))),
+        ("scales", lambda: Z.zpp_qwz_quant(u16(2 * n), 2, n, B, 4, u8(n), f32(2 * n // B - 1))),
+        ("y_bf16", lambda: Z.zpp_qwz_dequant(u8(2 * n), f32(2 * n // B), 2, n, B, 8, u16(n))),
+        ("grads_bf16", lambda: Z.zpp_qgz_reorder_quant(u16(nd * 4096 - 8), 2, 2, 4096, B, 4,
+                                                       u8(cb1), f32(nb1))),
+        ("codes", lambda: Z.zpp_qgz_reorder_quant(u16(nd * 4096), 2, 2, 4096, B, 4, u8(cb1 - 1),
+                                                  f32(nb1))),
+        ("acc", lambda: Z.zpp_qgz_reorder_quant_acc(u16(nd * 4096), f32(nd * 4096 - 1), 2, 2, 4096,
+                                                    B, 4, u8(cb1), f32(nb1))),
+        ("acc", lambda: Z.zpp_grad_accumulate(u16(100), f32(99), 100, 1)),
+        ("codes_in", lambda: Z.zpp_qgz_hop_reduce(1, u8(cb1 - 16), f32(nb1), 2, 2, 4096, B, 4,
+                                                  u8(cb2), f32(nb2))),
+        ("codes_out", lambda: Z.zpp_qgz_hop_reduce(1, u8(cb1), f32(nb1), 2, 2, 4096, B, 4,
+                                                   u8(cb2 - 1), f32(nb2))),
+        ("scales_in", lambda: Z.zpp_qgz_hop_reduce(2, u8(cb2), f32(nb2 - 1), 2, 2, 4096, B, 4,
+                                                   grad_out=f32(4096))),
+        ("grad_out", lambda: Z.zpp_qgz_hop_reduce(2, u8(cb2), f32(nb2), 2, 2, 4096, B, 4,
+                                                  grad_out=f32(4095))),
+        ("master", lambda: Z.zpp_qgz_hop_reduce(2, u8(cb2), f32(nb2), 2, 2, 4096, B, 4,
+                                                adam=(1e-4, .9, .999, 1e-8, 1), state=st(1))),
+        ("qwz_codes", lambda: Z.zpp_qgz_final_hop_adam_qwz(2, u8(cb2), f32(nb2), 2, 2, 4096, B, 4,
+                                                           None, (1e-4, .9, .999, 1e-8, 1), st(),
+                                                           8, u8(4095), f32(4096 // B))),
+        ("grads_bf16", lambda: Z.zpp_ring_rs_step(0, 4, 4096, B, 4, u16(4 * 4096 - 1),
+                                                  codes_out=u8(4 * 512), scales_out=f32(16))),
+        ("codes_out", lambda: Z.zpp_ring_rs_step(0, 4, 4096, B, 4, u16(4 * 4096),
+                                                 codes_out=u8(4 * 512 - 1), scales_out=f32(16))),
+        ("sec_codes[1]", lambda: Z.zpp_hpz_gather(2, 2, 1024, B, 8, [u8(2048), u8(2047)],
+                                                  [f32(8), f32(8)], u16(4096))),
+        ("y_bf16", lambda: Z.zpp_hpz_gather(2, 2, 1024, B, 8, [u8(2048), u8(2048)],
+                                            [f32(8), f32(8)], u16(4095))),
+        ("grad", lambda: Z.zpp_shard_adam_step(f32(99), 100, (1e-4, .9, .999, 1e-8, 1),
+                                               (f32(100), f32(100), f32(100), u16(100)))),
+        ("param_bf16", lambda: Z.zpp_shard_adam_step(f32(100), 100, (1e-4, .9, .999, 1e-8, 1),
+                                                     (f32(100), f32(100), f32(100), u16(99)))),
+    ]
+
+
+@pytest.mark.parametrize("i", range(20))
+def test_binding_rejects_undersized_tensors(i):
+    """An under-sized tensor raises ValueError naming it before any pointer is
+    taken or any call is made."""
+    name, call = _small_cases()[i]
+    with pytest.raises(ValueError, match=re.escape(name) + " is too small"):
+        call()
+
+
+def test_binding_size_check_accepts_exact_sizes():
+    """Exactly sized host tensors pass the size check and stop at the device
+    check (nothing reaches the library without a CUDA tensor)."""
+    import torch
+    import gradient_comm_codecs_gb300 as Z
+    n, B = 4096, 256
+    with pytest.raises(ValueError, match="must be on a CUDA device"):
+        Z.zpp_qwz_quant(torch.empty(2 * n, dtype=torch.bfloat16), 2, n, B, 4,
+                        torch.empty(n, dtype=torch.uint8), torch.empty(2 * n // B))

@@ -1,23 +1,31 @@
 """GPU parity at the workloads' full sizes, in the launch configuration the
-bench times (CodecPath), on sampled outputs the oracle recomputes one by one.
+bench times (CodecPath): every output element is compared with the oracle.
 
 Inputs are generated on the device by the counter-based generator; the host
-regenerates exactly the elements a sampled output depends on.  For qgZ a
-sampled block position b of every slice is a self-contained sub-problem: its
-one-shot codes, hop-1 partial sums and final gradient depend only on block b
-of every rank's slices, so the oracle runs the whole chain on a "mini bucket"
-made of the sampled blocks of all slices of all ranks and every rank's
-message, hop-1 message, reduced gradient and Adam state is compared there.
+regenerates them and the oracle recomputes the outputs in independent pieces
+side by side on the host cores (tests/fullcheck.py: qwZ shards split at block
+boundaries; for qgZ and the ring, groups of block positions of every slice of
+every rank form self-contained smaller buckets).
+
+The sweep's 144 points are all run: completely where N_d * bucket <= 2^28
+elements, and above that on sampled blocks (first, last and seeded random
+blocks of every slice and shard; a sampled block position b of every slice is
+a self-contained sub-problem, so the oracle runs the whole chain on the
+"mini bucket" of the sampled blocks).  A point is skipped only when its
+buffers do not fit in device memory, and the skip says so.
 """
 import numpy as np
 import pytest
 import torch
 
+import fullcheck as F
 import oracle
 import synth
 from synth import workloads as W
 from gpu_helpers import (assert_bf16_ulp, assert_bytes_equal, assert_f32_bitexact,
                          assert_grad_close, assert_rel_close, grads_for, zpp)
+
+COMPLETE_MAX_ELEMS = 1 << 28   # sweep points checked completely up to this N_d * bucket
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +53,8 @@ def sample_blocks(nblocks, k, seed):
     return sorted(picks)
 
 
-def build_path(Z, wl: W.Workload, keep_grad=True, fuse_qwz=False, microbatches=1):
+def build_path(Z, wl: W.Workload, keep_grad=True, fuse_qwz=False, microbatches=1,
+               standalone=False):
     q, g = wl.qwz, wl.qgz
     qs = gs = None
     if q is not None:
@@ -54,8 +63,9 @@ def build_path(Z, wl: W.Workload, keep_grad=True, fuse_qwz=False, microbatches=1
         gs = Z.QgzSpec(g.nodes, g.gpus_per_node, g.bucket, g.block, g.bits)
     a = wl.adam
     adam = Z.AdamSpec(a.lr, a.beta1, a.beta2, a.eps, a.step) if (g and wl.fused_adam) else None
+    sa = wl.standalone_adam if (standalone and adam is not None) else 0
     path = Z.CodecPath(qs, gs, adam, device="cuda", keep_grad=keep_grad, fuse_qwz=fuse_qwz,
-                       microbatches=microbatches)
+                       microbatches=microbatches, standalone_adam=sa)
     if q is not None:
         synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, qs.phi, out=path.w)
     if g is not None:
@@ -65,7 +75,32 @@ def build_path(Z, wl: W.Workload, keep_grad=True, fuse_qwz=False, microbatches=1
             m = synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, g.bucket, device="cuda")
             path.master.copy_(m.float())
             del m
+    if sa:   # the bench's standalone shard: N(0, 1e-3) gradients, weights after the bucket
+        t = synth.fill(W.GRAD_NORMAL, wl.seed, synth.SHARD_GRAD, 0, sa, device="cuda")
+        path.sa_grad.copy_(t.float())
+        synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, g.bucket, sa, out=t)
+        path.sa_master.copy_(t.float())
+        del t
     return path
+
+
+def run_checked(path, wl, *, fused_prime=False):
+    """One pass with every output compared completely with the oracle."""
+    cap = F.QwzCapture(path, wl) if path.qwz is not None else None
+    if fused_prime:
+        path.prime_fused_qwz()
+    path.run(mark=cap)
+    torch.cuda.synchronize()
+    if cap is not None:
+        cap.finish()
+    if path.qgz is not None:
+        F.check_qgz_complete(path, wl)
+    if path.standalone_adam:
+        a = wl.adam
+        F.check_adam_complete((path.sa_master, path.sa_m, path.sa_v, path.sa_param),
+                              path.standalone_adam, wl.seed,
+                              (a.lr, a.beta1, a.beta2, a.eps, a.step), W.GRAD_NORMAL,
+                              synth.SHARD_GRAD, master_start=wl.qgz.bucket, moments=False)
 
 
 def check_qwz(path, wl, nsample=3):
@@ -188,16 +223,13 @@ def check_qgz(path, wl, nsample=2):
 
 @pytest.mark.parametrize("name", ["tiny", "llama", "two_hop", "7b"])
 def test_workload_full_size(name):
+    """The bench's pass of each workload (the 7B one with its standalone Adam
+    shard), every output element against the oracle."""
     Z = zpp()
     wl = W.WORKLOADS[name]
     torch.cuda.empty_cache()
-    path = build_path(Z, wl)
-    path.run()
-    torch.cuda.synchronize()
-    if wl.qwz is not None:
-        check_qwz(path, wl)
-    if wl.qgz is not None:
-        check_qgz(path, wl)
+    path = build_path(Z, wl, standalone=True)
+    run_checked(path, wl)
     del path
     torch.cuda.empty_cache()
 
@@ -209,10 +241,7 @@ def test_llama_fused_adam_qwz_full_size():
     wl = W.WORKLOADS["llama"]
     torch.cuda.empty_cache()
     path = build_path(Z, wl, fuse_qwz=True)
-    path.prime_fused_qwz()
-    path.run()
-    torch.cuda.synchronize()
-    check_qgz(path, wl)
+    run_checked(path, wl, fused_prime=True)
     del path
     torch.cuda.empty_cache()
 
@@ -221,20 +250,19 @@ def test_llama_fused_adam_qwz_full_size():
 def test_gradient_accumulation_full_size(name, microbatches):
     """Gradient accumulation over micro-batches before the qgZ reduce: the
     accumulator after M-1 micro-batches, the one-shot messages of the
-    accumulated bucket, the hops and the fused Adam on sampled blocks."""
+    accumulated bucket, the hops and the fused Adam, every element."""
     Z = zpp()
     wl = W.WORKLOADS[name]
     torch.cuda.empty_cache()
     path = build_path(Z, wl, microbatches=microbatches)
-    path.run()
-    torch.cuda.synchronize()
-    check_qgz(path, wl)
+    run_checked(path, wl)
     del path
     torch.cuda.empty_cache()
 
 
 def test_7b_standalone_adam_full_size():
-    """Standalone Adam on the 7B workload's 109,375,000-parameter owned shard."""
+    """Standalone Adam on the 7B workload's 109,375,000-parameter owned shard
+    at step 7 from drawn moments, every element."""
     Z = zpp()
     n = W.SEVEN_B.standalone_adam
     g = synth.fill(W.GRAD_NORMAL, 3, synth.grad_stream(0), 0, n, device="cuda").float()
@@ -243,38 +271,37 @@ def test_7b_standalone_adam_full_size():
     v = synth.fill(W.MOMENT_V_RECIPE, 3, synth.MOMENT_V, 0, n, device="cuda").float()
     param = torch.empty(n, dtype=torch.bfloat16, device="cuda")
     hp = (1e-4, 0.9, 0.999, 1e-8, 7)
-    idx = np.unique(np.concatenate([np.arange(0, 1000), np.arange(n - 1000, n),
-                                    np.random.default_rng(5).integers(0, n, 20000)]))
-    g0, p0, m0, v0 = (gather_f32(t, idx) for t in (g, master, m, v))
     Z.zpp_shard_adam_step(g, n, hp, (master, m, v, param))
     torch.cuda.synchronize()
-    wp, wm, wv, wb = oracle.adam_step(g0, p0, m0, v0, *hp)
-    assert_rel_close(gather_f32(master, idx), wp, 1e-5, "master")
-    assert_rel_close(gather_f32(m, idx), wm, 1e-5, "m")
-    assert_rel_close(gather_f32(v, idx), wv, 1e-5, "v")
-    assert_bf16_ulp(gather_u16(param, idx), wb, "param")
+    del g
+    F.check_adam_complete((master, m, v, param), n, 3, hp, W.GRAD_NORMAL, synth.grad_stream(0))
 
 
-SWEEP_SAMPLE = [0, 7, 20, 30, 47, 50, 70, 95, 101, 118, 131, 141]
+def sweep_need_bytes(wl):
+    g, q = wl.qgz, wl.qwz
+    c = g.bits / 8 + 4 / g.block
+    return g.nd * g.bucket * (2 + c + c / g.gpus_per_node + 4 / g.nd) + q.phi * (2 + 2 + c)
 
 
-@pytest.mark.parametrize("index", SWEEP_SAMPLE)
-def test_sweep_points(index):
-    """A spread of sweep points (every block size, both widths, every topology,
-    1 MiB to 1 GiB per rank where it fits), sampled as above, no Adam."""
+@pytest.mark.parametrize("index", range(144))
+def test_sweep_point(index):
+    """Every sweep point (no Adam): completely where N_d * bucket <= 2^28,
+    else on sampled blocks of every shard and slice."""
     Z = zpp()
     wl = dict(W.sweep_points())[index]
-    need = wl.qgz.nd * wl.qgz.bucket * (2 + 2 * wl.qgz.bits / 8 + 8 / wl.qgz.block) \
-        + wl.qwz.phi * 5
+    need = sweep_need_bytes(wl)
     free, _ = torch.cuda.mem_get_info()
-    if need > 0.8 * free:
-        pytest.skip(f"needs {need / 2**30:.0f} GiB")
+    if need > 0.85 * free:
+        pytest.skip(f"device memory: needs {need / 2**30:.0f} GiB of {free / 2**30:.0f} GiB free")
     torch.cuda.empty_cache()
     path = build_path(Z, wl, keep_grad=True)
-    path.run()
-    torch.cuda.synchronize()
-    check_qwz(path, wl, nsample=1)
-    check_qgz(path, wl, nsample=1)
+    if wl.qgz.nd * wl.qgz.bucket <= COMPLETE_MAX_ELEMS:
+        run_checked(path, wl)
+    else:
+        path.run()
+        torch.cuda.synchronize()
+        check_qwz(path, wl, nsample=1)
+        check_qgz(path, wl, nsample=1)
     del path
     torch.cuda.empty_cache()
 
@@ -291,21 +318,22 @@ def test_llama_hpz_backward_gather_full_size(nodes):
     torch.cuda.empty_cache()
     path = Z.CodecPath(qs, None, None, device="cuda", hpz=True)
     synth.fill(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, 0, qs.phi, out=path.w)
-    path.run_qwz()
+    cap = F.QwzCapture(path, wl)
+    path.run_qwz(mark=cap)
+    cap.finish()
     fwd = path.w_full.clone()
     path.w_full.zero_()
     path.run_hpz()
     torch.cuda.synchronize()
     assert torch.equal(path.w_full.view(torch.int16), fwd.view(torch.int16))
-    check_qwz(path, wl)
     del path, fwd
     torch.cuda.empty_cache()
 
 
 def test_two_hop_bucket_ring_reduce_scatter_full_size():
     """The quantized ring over the two-hop workload's 16 ranks of 2^28-element
-    buckets, checked on sampled blocks of every chunk: blocks restart at chunk
-    starts, so the ring over those blocks alone reproduces them exactly."""
+    buckets, every reduced-gradient float (blocks restart at chunk starts, so
+    the ring over a group of block positions alone reproduces them)."""
     Z = zpp()
     g = W.WORKLOADS["two_hop"].qgz
     nd, bucket, B, bits = g.nd, g.bucket, g.block, g.bits
@@ -322,16 +350,7 @@ def test_two_hop_bucket_ring_reduce_scatter_full_size():
         Z.zpp_ring_rs_step(step, nd, bucket, B, bits, x, ci, si, co, so,
                            grad if step == nd - 1 else None)
     torch.cuda.synchronize()
-    blocks = sample_blocks(nb, 3, 11)
-    nbk = len(blocks)
-    # mini bucket: rank r, chunk c, sampled block q
-    pos = (np.arange(nd)[:, None, None] * L + np.asarray(blocks)[None, :, None] * B
-           + np.arange(B)[None, None, :]).reshape(-1)
-    mini = np.concatenate([synth.bf16_to_u16(synth.at(g.grad, 0, synth.grad_stream(r), pos))
-                           for r in range(nd)])
-    want = oracle.ring_reduce_scatter(mini, nd, nd * nbk * B, B, bits)
-    gidx = (np.arange(nd)[:, None, None] * L + np.asarray(blocks)[None, :, None] * B
-            + np.arange(B)[None, None, :]).reshape(-1)
-    assert_f32_bitexact(gather_f32(grad, gidx), want, "ring gradient")
-    del x, bufs, grad
+    del x, bufs
+    F.check_ring_complete(grad, g, 0)
+    del grad
     torch.cuda.empty_cache()
