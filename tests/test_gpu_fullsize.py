@@ -7,12 +7,13 @@ side by side on the host cores (tests/fullcheck.py: qwZ shards split at block
 boundaries; for qgZ and the ring, groups of block positions of every slice of
 every rank form self-contained smaller buckets).
 
-The sweep's 144 points are all run: completely where N_d * bucket <= 2^28
+The sweep's 144 points are all run: completely where N_d * bucket <= 2^30
 elements, and above that on sampled blocks (first, last and seeded random
 blocks of every slice and shard; a sampled block position b of every slice is
 a self-contained sub-problem, so the oracle runs the whole chain on the
-"mini bucket" of the sampled blocks).  A point is skipped only when its
-buffers do not fit in device memory, and the skip says so.
+"mini bucket" of the sampled blocks).  A point too large for one pass runs
+its qgZ chain and its qwZ calls separately; a point is skipped only when its
+qgZ chain alone does not fit in device memory, and the skip says so.
 """
 import numpy as np
 import pytest
@@ -25,7 +26,7 @@ from synth import workloads as W
 from gpu_helpers import (assert_bf16_ulp, assert_bytes_equal, assert_f32_bitexact,
                          assert_grad_close, assert_rel_close, grads_for, zpp)
 
-COMPLETE_MAX_ELEMS = 1 << 28   # sweep points checked completely up to this N_d * bucket
+COMPLETE_MAX_ELEMS = 1 << 30   # sweep points checked completely up to this N_d * bucket
 
 pytestmark = pytest.mark.gpu
 
@@ -103,36 +104,31 @@ def run_checked(path, wl, *, fused_prime=False):
                               synth.SHARD_GRAD, master_start=wl.qgz.bucket, moments=False)
 
 
-def check_qwz(path, wl, nsample=3):
-    """Sampled blocks of every call's dequantized output; codes and scales of
-    the last call of each shard size (earlier calls of the same size reuse
-    that call's code buffer, as a streamed long tensor does)."""
+def check_qwz_sampled(codes, scales, y, nranks, shard, B, bits, seed, gstart, nsample=1):
+    """Sampled blocks (first, last, seeded random) of every rank's codes,
+    scales and dequantized weights of one qwZ call whose weights start at
+    global index gstart."""
+    nb = -(-shard // B)
+    cb = oracle.codes_bytes(shard, bits)
+    for r in range(nranks):
+        for b in sample_blocks(nb, nsample, 1000 + r):
+            n = min(B, shard - b * B)
+            lidx = r * shard + b * B + np.arange(n)
+            x = synth.at_u16(W.WEIGHT_RECIPE, seed, synth.WEIGHTS, gstart + lidx)
+            wc, ws = oracle.qwz_quant(x, 1, n, B, bits)
+            wy = oracle.qwz_dequant(wc, ws, 1, n, B, bits)
+            assert_bytes_equal(gather_u16(y, lidx), wy, f"qwZ dequant rank {r} block {b}")
+            got_c = gather_bytes(codes, [r * cb + (b * B * bits) // 8], wc.size)
+            assert_bytes_equal(got_c, wc, f"qwZ codes rank {r} block {b}")
+            assert_f32_bitexact(gather_f32(scales, [r * nb + b]), ws, f"qwZ scale rank {r} block {b}")
+
+
+def check_qwz(path, wl, nsample=1):
+    """Sampled blocks of every rank of a one-call qwZ pass."""
     q = wl.qwz
-    B, bits = q.block, q.bits
-    shards = path.qwz.call_shards()
-    last_of = {s: i for i, s in enumerate(shards)}
-    calls = sorted({0, len(shards) - 1, len(shards) // 2} | set(last_of.values()))
-    offs = np.concatenate([[0], np.cumsum([q.nranks * s for s in shards])])
-    for call in calls:
-        s, off = shards[call], int(offs[call])
-        i = path._codes_of[s]
-        codes, scales = path.w_codes[i], path.w_scales[i]
-        nb = -(-s // B)
-        cb = oracle.codes_bytes(s, bits)
-        for r in sorted({0, q.nranks - 1}):
-            for b in sample_blocks(nb, nsample, 1000 * call + r):
-                n = min(B, s - b * B)
-                gidx = off + r * s + b * B + np.arange(n)
-                x = synth.bf16_to_u16(synth.at(W.WEIGHT_RECIPE, wl.seed, synth.WEIGHTS, gidx))
-                wc, ws = oracle.qwz_quant(x, 1, n, B, bits)
-                wy = oracle.qwz_dequant(wc, ws, 1, n, B, bits)
-                assert_bytes_equal(gather_u16(path.w_full, gidx), wy, f"qwZ dequant {call}/{r}/{b}")
-                if last_of[s] != call:
-                    continue
-                got_c = gather_bytes(codes, [r * cb + (b * B * bits) // 8], wc.size)
-                assert_bytes_equal(got_c, wc, f"qwZ codes call {call} rank {r} block {b}")
-                got_s = gather_f32(scales, [r * nb + b])
-                assert_f32_bitexact(got_s, ws, f"qwZ scale call {call} rank {r} block {b}")
+    assert q.calls == 1
+    check_qwz_sampled(path.w_codes[0], path.w_scales[0], path.w_full, q.nranks, q.shard, q.block,
+                      q.bits, wl.seed, 0, nsample)
 
 
 def check_qgz(path, wl, nsample=2):
@@ -277,33 +273,75 @@ def test_7b_standalone_adam_full_size():
     F.check_adam_complete((master, m, v, param), n, 3, hp, W.GRAD_NORMAL, synth.grad_stream(0))
 
 
-def sweep_need_bytes(wl):
-    g, q = wl.qgz, wl.qwz
+def qgz_need_bytes(g):
     c = g.bits / 8 + 4 / g.block
-    return g.nd * g.bucket * (2 + c + c / g.gpus_per_node + 4 / g.nd) + q.phi * (2 + 2 + c)
+    return g.nd * g.bucket * (2 + c + c / g.gpus_per_node) + 4 * g.bucket
+
+
+def qwz_need_bytes(q, nranks=None):
+    c = q.bits / 8 + 4 / q.block
+    return (q.nranks if nranks is None else nranks) * q.shard * (2 + 2 + c)
+
+
+def run_qwz_rank_groups(Z, q, seed, ranks_per_call):
+    """The qwZ half of a sweep point too large for one call's buffers: its
+    shards are independent, so they run as calls over groups of ranks (each
+    with its weights at the group's global offset), checked on sampled
+    blocks of every rank."""
+    cb, nb = Z.zpp_codes_bytes(q.shard, q.bits), Z.zpp_num_blocks(q.shard, q.block)
+    for r0 in range(0, q.nranks, ranks_per_call):
+        n = min(ranks_per_call, q.nranks - r0)
+        w = torch.empty(n * q.shard, dtype=torch.bfloat16, device="cuda")
+        synth.fill(W.WEIGHT_RECIPE, seed, synth.WEIGHTS, r0 * q.shard, n * q.shard, out=w,
+                   chunk=1 << 27)
+        codes = torch.empty(n * cb, dtype=torch.uint8, device="cuda")
+        scales = torch.empty(n * nb, device="cuda")
+        Z.zpp_qwz_quant(w, n, q.shard, q.block, q.bits, codes, scales)
+        Z.zpp_qwz_dequant(codes, scales, n, q.shard, q.block, q.bits, w)   # in place: w is y now
+        torch.cuda.synchronize()
+        check_qwz_sampled(codes, scales, w, n, q.shard, q.block, q.bits, seed, r0 * q.shard)
+        del w, codes, scales
+        torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("index", range(144))
 def test_sweep_point(index):
-    """Every sweep point (no Adam): completely where N_d * bucket <= 2^28,
-    else on sampled blocks of every shard and slice."""
+    """Every sweep point (no Adam): completely where N_d * bucket <= 2^30
+    elements, else on sampled blocks of every shard and slice.  A point whose
+    buffers do not fit in one pass runs its qgZ chain and its qwZ calls
+    separately (the qwZ shards in groups of ranks); only a qgZ chain that does
+    not fit by itself is skipped."""
+    import dataclasses
     Z = zpp()
     wl = dict(W.sweep_points())[index]
-    need = sweep_need_bytes(wl)
-    free, _ = torch.cuda.mem_get_info()
-    if need > 0.85 * free:
-        pytest.skip(f"device memory: needs {need / 2**30:.0f} GiB of {free / 2**30:.0f} GiB free")
+    g, q = wl.qgz, wl.qwz
     torch.cuda.empty_cache()
-    path = build_path(Z, wl, keep_grad=True)
-    if wl.qgz.nd * wl.qgz.bucket <= COMPLETE_MAX_ELEMS:
-        run_checked(path, wl)
-    else:
-        path.run()
-        torch.cuda.synchronize()
-        check_qwz(path, wl, nsample=1)
-        check_qgz(path, wl, nsample=1)
+    budget = 0.85 * torch.cuda.mem_get_info()[0]
+    complete = g.nd * g.bucket <= COMPLETE_MAX_ELEMS
+    if qgz_need_bytes(g) + qwz_need_bytes(q) <= budget:
+        path = build_path(Z, wl, keep_grad=True)
+        if complete:
+            run_checked(path, wl)
+        else:
+            path.run()
+            torch.cuda.synchronize()
+            check_qwz(path, wl, nsample=1)
+            check_qgz(path, wl, nsample=1)
+        del path
+        torch.cuda.empty_cache()
+        return
+    assert not complete
+    if qgz_need_bytes(g) > budget:
+        pytest.skip(f"device memory: the qgZ chain needs {qgz_need_bytes(g) / 2**30:.0f} GiB, "
+                    f"{budget / 0.85 / 2**30:.0f} GiB free")
+    path = build_path(Z, dataclasses.replace(wl, qwz=None), keep_grad=True)
+    path.run()
+    torch.cuda.synchronize()
+    check_qgz(path, wl, nsample=1)
     del path
     torch.cuda.empty_cache()
+    budget = 0.85 * torch.cuda.mem_get_info()[0]
+    run_qwz_rank_groups(Z, q, wl.seed, max(1, int(budget // qwz_need_bytes(q, 1))))
 
 
 @pytest.mark.parametrize("nodes", [1, 2, 4])

@@ -406,7 +406,7 @@ def test_final_hop_adam_qwz_rejects_unsupported():
     N, G, block, bits = 1, 4, 256, 4
     bucket = 4 * 768                        # L = 768: not a multiple of 512
     t = torch.zeros(bucket, device="cuda")
-    c = torch.zeros(bucket, dtype=torch.uint8, device="cuda")
+    c = torch.zeros(4 * bucket, dtype=torch.uint8, device="cuda")
     st = (t, t.clone(), t.clone(), None)
     with pytest.raises(Z.ZppError) as e:
         Z.zpp_qgz_final_hop_adam_qwz(1, c, t, N, G, bucket, block, bits, None,
@@ -414,7 +414,7 @@ def test_final_hop_adam_qwz_rejects_unsupported():
     assert e.value.status == Z.ZPP_ERR_UNSUPPORTED
     bucket = 4 * 1024
     t = torch.zeros(bucket, device="cuda")
-    c = torch.zeros(bucket, dtype=torch.uint8, device="cuda")
+    c = torch.zeros(4 * bucket, dtype=torch.uint8, device="cuda")
     with pytest.raises(Z.ZppError) as e:
         Z.zpp_qgz_final_hop_adam_qwz(1, c, t, N, G, bucket, block, bits, None,
                                      (1e-4, 0.9, 0.999, 1e-8, 1), (t, t.clone(), t.clone(), None),
@@ -491,15 +491,15 @@ def test_qgz_reorder_quant_acc(bits, block, slice_blocks, N, G, M):
 
 def test_accumulation_arguments():
     Z = zpp()
-    g = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
-    acc = torch.zeros(65, device="cuda")
+    g = torch.zeros(128, dtype=torch.bfloat16, device="cuda")
+    acc = torch.zeros(129, device="cuda")
     with pytest.raises(Z.ZppError) as e:
         Z.zpp_grad_accumulate(g, acc, 64, 2)
     assert e.value.status == Z.ZPP_ERR_INVALID_ARG
     with pytest.raises(Z.ZppError) as e:
         Z.zpp_grad_accumulate(g, acc[1:], 64, 1)
     assert e.value.status == Z.ZPP_ERR_MISALIGNED
-    c = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    c = torch.zeros(128, dtype=torch.uint8, device="cuda")
     with pytest.raises(Z.ZppError) as e:   # bucket not a multiple of N_d * block
         Z.zpp_qgz_reorder_quant_acc(g, acc, 1, 2, 64, 64, 8, c, acc)
     assert e.value.status == Z.ZPP_ERR_INVALID_ARG
@@ -628,8 +628,9 @@ def test_hpz_arguments():
             Z.ZPP_ERR_INVALID_ARG, args
     assert lib.zpp_hpz_gather(2, 1, 4096, 64, 8, P(cp), None, y.data_ptr(), None) == \
         Z.ZPP_ERR_INVALID_ARG
+    cm = torch.zeros(4096 + 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(Z.ZppError) as e:
-        Z.zpp_hpz_gather(2, 1, 4096, 64, 8, [c[0], c[1][4:]], s, y)
+        Z.zpp_hpz_gather(2, 1, 4096, 64, 8, [c[0], cm[4:4100]], s, y)
     assert e.value.status == Z.ZPP_ERR_MISALIGNED
     assert Z.zpp_hpz_secondary_bytes(2, 4096, 256, 8) == oracle.hpz_secondary_bytes(2, 4096, 256, 8)
     assert Z.zpp_hpz_secondary_bytes(2, 4096, 256, 16) == 2 * 2 * 4096
@@ -687,8 +688,8 @@ def test_ring_reduce_scatter(bits, block, chunk_blocks, nd):
 
 def test_ring_arguments():
     Z = zpp()
-    x = torch.zeros(4 * 256, dtype=torch.bfloat16, device="cuda")
-    c = torch.zeros(512, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(4 * 1024, dtype=torch.bfloat16, device="cuda")
+    c = torch.zeros(1024, dtype=torch.uint8, device="cuda")
     s = torch.zeros(16, device="cuda")
     g = torch.zeros(4 * 256, device="cuda")
     Z.zpp_ring_rs_step(0, 2, 512, 64, 8, x, None, None, c, s)
