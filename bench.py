@@ -732,8 +732,12 @@ def run_ring_sweep(args):
 def run_sweep(args):
     """Every sweep point: qgZ chain (reorder+quant, hop 1, hop 2 / final, no
     Adam) and qwZ quant+dequant on N_d shards of the same size, timed with
-    CUDA events (plain launches) and, for the qgZ chain, as a CUDA-graph
-    replay.  Timing inputs are filled in place by torch's normal_ (bf16,
+    CUDA events (plain launches back to back, so points smaller than L2 run
+    from L2) and, for the qgZ chain, as a CUDA-graph replay, and once more
+    with L2 flushed before every pass (a read of twice L2's size) and an
+    event after every kernel (the per-kernel split, in microseconds).  The
+    first line is the launch floor: a one-element kernel's time on the
+    stream.  Timing inputs are filled in place by torch's normal_ (bf16,
     N(0, 1e-3) gradients, N(0, 0.02) weights); parity of sweep points is
     covered by the tests.  Points whose buffers do not fit in free memory are
     skipped and reported as such."""
@@ -745,6 +749,22 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     out = []
+    flush = None
+    # the launch floor: a one-element kernel, back to back, timed the same way
+    st0 = torch.cuda.current_stream(dev)
+    one = torch.zeros(1, device=dev)
+    for _ in range(10):
+        one.add_(1)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(st0)
+    for _ in range(200):
+        one.add_(1)
+    a1.record(st0)
+    torch.cuda.synchronize()
+    floor = {"launch_floor_us": 1e3 * a0.elapsed_time(a1) / 200,
+             "note": "a one-element torch kernel launched 200 times back to back: the time a "
+                     "launch takes on the stream when there is no work"}
+    print(json.dumps(floor), flush=True)
     for i, wl in W.sweep_points():
         q, g = wl.qwz, wl.qgz
         if g.bucket * 2 > args.sweep_max_mib << 20:
@@ -783,6 +803,33 @@ def run_sweep(args):
         ms = e0.elapsed_time(e1) / iters
         rec.update(qgz_ms=ms, qgz_gbs=qgz_bytes / (ms * 1e-3) / 1e9,
                    qgz_elems_per_s=nd * b / (ms * 1e-3))
+        # per-kernel split, and the chain again with L2 flushed before every pass
+        # (a read of twice L2's size, so L2 holds only clean lines of another
+        # buffer when the chain starts), the chain timed alone
+        per = {}
+        if flush is None:
+            flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+        reps = max(3, min(50, iters))
+        t_flushed = 0.0
+        for _ in range(reps):
+            flush.sum()
+            marks = [torch.cuda.Event(enable_timing=True)]
+            marks[0].record(st)
+
+            def mark(name, marks=marks):
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(st)
+                marks.append((name, ev))
+            path.run_qgz(st, mark=mark)
+            torch.cuda.synchronize()
+            prev = marks[0]
+            for name, ev in marks[1:]:
+                per.setdefault(name, []).append(prev.elapsed_time(ev))
+                prev = ev
+            t_flushed += marks[0].elapsed_time(marks[-1][1])
+        rec["qgz_flushed_ms"] = t_flushed / reps
+        rec["qgz_flushed_gbs"] = qgz_bytes / (t_flushed / reps * 1e-3) / 1e9
+        rec["kernels_flushed_us"] = {n: 1e3 * sum(v) / len(v) for n, v in per.items()}
         # CUDA-graph replay of the same chain (launch overhead removed)
         gs = torch.cuda.Stream(dev)
         gs.wait_stream(st)

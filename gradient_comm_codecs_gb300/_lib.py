@@ -150,13 +150,19 @@ def _nb(n, block):
     return -(-n // block)
 
 
+_NULL = contextlib.nullcontext()
+
+
 def _guard(where, *needs):
     """Check every (tensor, bytes needed, name) of a call and return a context
-    that makes the tensors' device current.  Sizes are only checked when the
-    scalar arguments are well formed; malformed ones are left for the
-    library's own validation (it returns ZPP_ERR_INVALID_ARG)."""
+    that makes the tensors' device current (a no-op context when it already
+    is).  Sizes are only checked when the scalar arguments are well formed;
+    malformed ones are left for the library's own validation (it returns
+    ZPP_ERR_INVALID_ARG)."""
     dev = None
     for t, need, name in needs:
+        if t is None or type(t) is int:
+            continue
         if not isinstance(t, torch.Tensor):
             continue
         if t.is_cuda:
@@ -164,18 +170,24 @@ def _guard(where, *needs):
                 dev = t.device
             elif t.device != dev:
                 raise ValueError(f"{where}: {name} is on {t.device}, other arguments on {dev}")
-        if need is not None and need > 0:
+        if need:
             have = t.numel() * t.element_size()
             if have < need:
                 raise ValueError(f"{where}: {name} is too small: {have} bytes, the call "
                                  f"accesses {need}")
-    return torch.cuda.device(dev) if dev is not None else contextlib.nullcontext()
+    if dev is None or dev.index == torch.cuda.current_device():
+        return _NULL
+    return torch.cuda.device(dev)
 
 
 def _ok(*vals):
-    """True when every size argument is a non-negative int and every block /
-    bit width is usable for the size rules."""
-    return all(isinstance(v, numbers.Integral) and v >= 0 for v in vals)
+    """True when every size argument is a non-negative integer."""
+    for v in vals:
+        if type(v) is not int and not isinstance(v, numbers.Integral):
+            return False
+        if v < 0:
+            return False
+    return True
 
 
 def _codec_ok(block, bits):

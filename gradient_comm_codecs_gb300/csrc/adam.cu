@@ -73,10 +73,10 @@ cudaError_t launch_adam(const float* grad, int64_t n, const AdamConstsHost& ac, 
   const int64_t ctas = (units + kWarps - 1) / kWarps;
   if (aligned32(grad) && aligned32(master) && aligned32(m) && aligned32(v)) {
     const void* k = reinterpret_cast<const void*>(&adam_kernel<true>);
-    adam_kernel<true><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+    adam_kernel<true><<<grid_for(k, ctas, 0, kStreamWaves), kThreads, 0, st>>>(a);
   } else {
     const void* k = reinterpret_cast<const void*>(&adam_kernel<false>);
-    adam_kernel<false><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
+    adam_kernel<false><<<grid_for(k, ctas, 0, kStreamWaves), kThreads, 0, st>>>(a);
   }
   return cudaGetLastError();
 }

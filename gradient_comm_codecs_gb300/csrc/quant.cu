@@ -394,7 +394,8 @@ cudaError_t run_quant(const QuantArgs& a0, int block, cudaStream_t st) {
       const void* k = reinterpret_cast<const void*>(&quant_tiled_kernel<BITS, REORDER, LOGB, ACC>);
       const cudaError_t attr = smem_opt_in(k, smem);
       if (attr != cudaSuccess) return attr;
-      quant_tiled_kernel<BITS, REORDER, LOGB, ACC><<<grid_for(k, ctas, smem), kThreads, smem, st>>>(a);
+      quant_tiled_kernel<BITS, REORDER, LOGB, ACC>
+          <<<grid_for(k, ctas, smem, kStreamWaves), kThreads, smem, st>>>(a);
     } else {
       const void* k = reinterpret_cast<const void*>(&quant_kernel<BITS, REORDER, LOGB, ACC>);
       quant_kernel<BITS, REORDER, LOGB, ACC><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
@@ -408,14 +409,14 @@ cudaError_t run_dequant(const DequantArgs& a0, int block, cudaStream_t st) {
   if constexpr (BITS == 16) {  // a copy: the block size plays no part
     const void* k = reinterpret_cast<const void*>(&dequant_kernel<16, 12>);
     dequant_kernel<16, 12>
-        <<<grid_for(k, (a0.total_units + kWarps - 1) / kWarps), kThreads, 0, st>>>(a0);
+        <<<grid_for(k, (a0.total_units + kWarps - 1) / kWarps, 0, kStreamWaves), kThreads, 0, st>>>(a0);
     return cudaGetLastError();
   } else {
     return dispatch_logb(block, [&](auto lb) -> cudaError_t {
       constexpr int LOGB = decltype(lb)::value;
       const void* k = reinterpret_cast<const void*>(&dequant_kernel<BITS, LOGB>);
       dequant_kernel<BITS, LOGB>
-          <<<grid_for(k, (a0.total_units + kWarps - 1) / kWarps), kThreads, 0, st>>>(a0);
+          <<<grid_for(k, (a0.total_units + kWarps - 1) / kWarps, 0, kStreamWaves), kThreads, 0, st>>>(a0);
       return cudaGetLastError();
     });
   }
@@ -453,7 +454,8 @@ cudaError_t launch_grad_accumulate(const uint16_t* g, float* acc, int64_t n, int
                                    cudaStream_t st) {
   const void* k = reinterpret_cast<const void*>(&accumulate_kernel);
   const int64_t ctas = (n + (int64_t)kThreads * 8 - 1) / ((int64_t)kThreads * 8);
-  accumulate_kernel<<<grid_for(k, ctas), kThreads, 0, st>>>(g, acc, n, first, aligned32(acc));
+  accumulate_kernel<<<grid_for(k, ctas, 0, kStreamWaves), kThreads, 0, st>>>(g, acc, n, first,
+                                                                         aligned32(acc));
   return cudaGetLastError();
 }
 

@@ -84,7 +84,7 @@ zpp_status check_topology(int32_t nodes, int32_t gpn, int64_t bucket, int32_t bl
 
 }  // namespace
 
-int grid_for(const void* kernel, int64_t work_ctas, size_t smem) {
+int grid_for(const void* kernel, int64_t work_ctas, size_t smem, int waves) {
   static std::mutex mu;
   static std::unordered_map<uint64_t, int> cache;  // (kernel, device) -> resident CTAs
   int dev = 0;
@@ -104,7 +104,8 @@ int grid_for(const void* kernel, int64_t work_ctas, size_t smem) {
     std::lock_guard<std::mutex> lock(mu);
     cache[key] = total;
   }
-  int64_t g = work_ctas < total ? work_ctas : total;
+  const int64_t cap = (int64_t)total * (waves > 1 ? waves : 1);
+  int64_t g = work_ctas < cap ? work_ctas : cap;
   return g < 1 ? 1 : (int)g;
 }
 

@@ -69,8 +69,25 @@ cudaError_t launch_ring_rs_step(int32_t step, int32_t nd, int64_t bucket, int32_
 cudaError_t launch_adam(const float* grad, int64_t n, const AdamConstsHost& ac, float* master,
                         float* m, float* v, uint16_t* param, cudaStream_t st);
 
-// Grid size for a kernel: min(work CTAs, SMs * resident CTAs per SM).
-int grid_for(const void* kernel, int64_t work_ctas, size_t smem = 0);
+// Grid size for a kernel: min(work CTAs, waves * SMs * resident CTAs per SM).
+// waves = 1: a persistent grid, every CTA resident at once, each warp group
+// walking a fixed contiguous range of units.  waves > 1: up to that many
+// rounds of resident CTAs, each CTA taking a smaller range; the hardware
+// hands the next CTA to whichever SM frees a slot first, so SMs that stream
+// faster take more of the work and the grid ends together instead of waiting
+// on the slowest fixed range.
+int grid_for(const void* kernel, int64_t work_ctas, size_t smem = 0, int waves = 1);
+
+// Rounds of resident CTAs for the streaming kernels (quantize, dequantize,
+// standalone Adam, accumulation), measured on GB300 over 1, 8, 16, 24, 32 and
+// 64 rounds: with 8, in the 7B step the qwZ quantizer went from 0.82 to 0.95
+// of the copy peak, the dequantizer 0.91 -> 0.99, the reorder quantizer
+// 0.94 -> 1.00 and Adam 0.97 -> 0.99; from 24 rounds on the quantizers lose
+// again (a warp group then gets one or two units, and each CTA's start-up --
+// its first copies in flight -- is no longer amortised).  The hop kernels
+// (two CTAs an SM, heavy per-CTA set-up) stay persistent: no round count
+// changed them.
+constexpr int kStreamWaves = 8;
 
 // Raises the kernel's dynamic shared-memory limit to `smem` bytes on the
 // current device, once per (kernel, device); a failure is returned and not
