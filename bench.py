@@ -398,6 +398,17 @@ def run_gpu(args, wl, rank, world, device):
         prev = ev
     ms_step = max_over_ranks(total_ms / args.steps, device)
 
+    # the same steps once more with events only around them (after the timed region, for
+    # information): what the events between kernels cost the step
+    bare = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    bare[0].record(stream)
+    for i in range(args.steps):
+        one_step(args.warmup + args.steps + i)
+    bare[1].record(stream)
+    torch.cuda.synchronize()
+    ms_step_bare = bare[0].elapsed_time(bare[1]) / args.steps
+
     peak, peak_kind = measured_peak()
     kernels = {}
     bytes_of = {}
@@ -443,6 +454,7 @@ def run_gpu(args, wl, rank, world, device):
         "pct_hbm_peak_nominal": 100.0 * value / world / NOMINAL_HBM_GBS,
         "qgz_bucket_elems_per_s": qgz_eps * world if qgz_eps else None,
         "bytes_per_step": step_bytes,
+        "ms_per_step_without_kernel_events": ms_step_bare,
         "gpu_launches": sum(len(v) for v in per.values()),
         "kernels": kernels, "roofline": roofline, "clocks": clocks, "e2e": e2e,
         "impl": "ours",
