@@ -407,7 +407,9 @@ __global__ void __launch_bounds__(kThreads, 2) hop_tiled_kernel(const HopArgs a)
 //
 // Chunks whose scales are all below 2^-5 (a warp vote) are dequantized by one
 // FMA a code (dequant_acc_i4 / dequant_acc_i8); others by the magic-number
-// decode.
+// decode.  int4 with eight sources takes hop1_staged_kernel below instead; this
+// kernel serves int8 (whose stages would leave one CTA an SM) and other source
+// counts.
 template <int BITS, int LOGB, int SCH>
 __global__ void __launch_bounds__(kThreads, 2) hop1_kernel(const HopArgs a) {
   using G = Geo<LOGB, 4>;
@@ -530,6 +532,172 @@ __global__ void __launch_bounds__(kThreads, 2) hop1_kernel(const HopArgs a) {
   }
 }
 
+// Hop 1 for int4 with eight sources, the codes staged in shared memory.  Same
+// lane layout and arithmetic as hop1_kernel (a lane owns 32 consecutive
+// elements of its warp's 1024; sources summed in rank order), but the sources
+// of the next unit are brought in by cp.async while this unit is summed:
+//  - each lane copies its own 16-byte code vector of every source into a
+//    slot it alone reads back, so the codes need no cross-lane sync;
+//  - the warp slab's 1024/B scales of a source (at least one) are copied by
+//    the first lanes and read by all, behind a __syncwarp;
+//  - two stages a warp: unit u+1 is copied while unit u is summed, and a
+//    stage is refilled only after every lane has read it (the __syncwarp at
+//    the end of a unit).
+// With no code registers held across units the kernel needs 80 registers, so
+// three CTAs (24 warps) fit an SM next to their 3 x 66 KB of stages, and
+// cp.async.wait_group is a hardware wait: on GB300 the long-scoreboard stalls
+// per issue fall from 1.19 to 0.25 against hop1_kernel and issue goes from 62%
+// to 68% active, for 2% more instructions (the copies and the shared-memory
+// reads); what is left is the decode's ALU work.  The first source of a unit
+// is written straight into the accumulator (dequant_set_i4).
+// acc[i] = RN(q_i s), i = 0..7: the first source of a sum written straight
+// into the accumulator instead of added to a zero one.  The two differ only
+// where RN(q s) is -0 (0 + -0 is +0), and a requantizing sum cannot tell: the
+// block absmax takes |x| and a zero quantizes to code 0 either way.  Requires
+// s < 2^-5, like dequant_acc_i4.
+__device__ __forceinline__ void dequant_set_i4(uint32_t w, const I4Fma& k, float* acc) {
+  const uint32_t x = w ^ 0x88888888u;
+  const uint32_t ev = x & 0x0F0F0F0Fu, od = (x >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 dq = __ffma2_rn(i4_subnormal_pair(ev, od, j), k.sp, k.c);
+    acc[2 * j] = dq.x;
+    acc[2 * j + 1] = dq.y;
+  }
+}
+
+constexpr int kStagedSources = 8;
+constexpr int kHop1StagedRounds = 4;  // CTA rounds (grid_for): 0.576 / 0.589 / 0.593 of the
+                                      // copy peak for 1 / 2 / 4 on the two-hop bucket
+
+template <int LOGB>
+__host__ __device__ constexpr int hop1_scale_slot() {  // a warp's scales of one source, padded
+  return LOGB <= 8 ? 16 << (8 - LOGB) : 16;
+}
+template <int LOGB>
+__host__ __device__ constexpr int hop1_stage_bytes() {  // one warp's stage
+  return kStagedSources * (32 * 16 + hop1_scale_slot<LOGB>());
+}
+
+template <int LOGB>
+__global__ void __launch_bounds__(kThreads, 3) hop1_staged_kernel(const HopArgs a) {
+  constexpr int BITS = 4, S = kStagedSources;
+  using G = Geo<LOGB, 4>;
+  constexpr int WPB = G::WPB, GPC = kWarps / WPB;
+  constexpr int QMAX = 7;
+  constexpr int LCB = 16;                              // a lane's code bytes of one source
+  constexpr int SRC = 32 * LCB + hop1_scale_slot<LOGB>();  // one source in a stage
+  constexpr int STAGE = hop1_stage_bytes<LOGB>();
+  constexpr int NSC = LOGB <= 10 ? (1024 >> LOGB) : 1;  // scales of a warp slab (at least one)
+  constexpr unsigned kAll = 0xffffffffu;
+  extern __shared__ __align__(128) uint8_t stages[];
+  __shared__ float red[2][kWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = warp / WPB, wsub = warp - gid * WPB;
+
+  int64_t u, uend;
+  unit_range(a.total_units, (int64_t)blockIdx.x * GPC + gid, (int64_t)gridDim.x * GPC, u, uend);
+  if (u >= uend) return;
+  uint8_t* const wstage = stages + (size_t)warp * 2 * STAGE;
+  const int64_t d0 = u / a.units_per_row;
+  int64_t t = u - d0 * a.units_per_row;
+  int32_t dn = (int32_t)(d0 / a.G), dl = (int32_t)(d0 - (int64_t)dn * a.G);
+  const int64_t cstep = (a.in_rank_elems * BITS) >> 3;  // bytes between consecutive sources
+  const int64_t fstep = a.in_rank_elems >> LOGB;        // scales between consecutive sources
+  const int lane_e = 32 * lane;
+  const int my_sc = LOGB <= 10 ? (lane_e >> LOGB) : 0;  // the lane's scale in its slab's
+  // copies of unit (n, l, tt), all S sources, into stage `st`
+  auto issue = [&](int st, int32_t n, int32_t l, int64_t tt) {
+    const int64_t e0 = (int64_t)n * a.G * a.in_rank_elems + (int64_t)l * a.R + tt * G::U +
+                       (int64_t)wsub * G::kWarpElems;
+    const uint8_t* cw = a.codes_in + ((e0 * BITS) >> 3) + lane * LCB;
+    const float* sw = a.scales_in + (e0 >> LOGB);  // 16-byte aligned: e0 is a multiple of 1024
+    uint8_t* dst = wstage + st * STAGE;
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      cp_async16(dst + j * SRC + lane * LCB, cw + (int64_t)j * cstep);
+      uint8_t* sdst = dst + j * SRC + 32 * LCB;
+      const float* ssrc = sw + (int64_t)j * fstep;
+      if constexpr (NSC >= 4) {
+        if (lane < NSC / 4) cp_async16(sdst + 16 * lane, ssrc + 4 * lane);
+      } else if (lane == 0) {
+        if constexpr (NSC == 2)
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(sdst)), "l"(ssrc)
+                       : "memory");
+        else
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sdst)), "l"(ssrc)
+                       : "memory");
+      }
+    }
+  };
+  auto next_unit = [&](int64_t& tt, int32_t& n, int32_t& l) {
+    if (++tt == a.units_per_row) {
+      tt = 0;
+      if (++l == a.G) {
+        l = 0;
+        ++n;
+      }
+    }
+  };
+
+  issue(0, dn, dl, t);
+  cp_async_commit();
+  int64_t t1 = t;  // (t1, dn1, dl1): the unit after the current one
+  int32_t dn1 = dn, dl1 = dl;
+  next_unit(t1, dn1, dl1);
+  float acc[4][8];
+  const float2 one2 = make_float2(a.one, a.one);
+  for (int64_t q = 0; u < uend; ++u, ++q) {
+    const int st = (int)(q & 1), parity = st;
+    if (u + 1 < uend) issue(st ^ 1, dn1, dl1, t1);  // read during the unit before this one
+    cp_async_commit();
+    cp_async_wait<1>();  // this unit's copies have landed
+    __syncwarp();        // and so have the other lanes' scale copies
+    const uint8_t* src = wstage + st * STAGE;
+    float sc[S];
+#pragma unroll
+    for (int j = 0; j < S; ++j) sc[j] = reinterpret_cast<const float*>(src + j * SRC + 32 * LCB)[my_sc];
+    float smax = sc[0];
+#pragma unroll
+    for (int j = 1; j < S; ++j) smax = fmaxf(smax, sc[j]);
+    if (__all_sync(kAll, smax < kFmaDequantMaxScale)) {
+#pragma unroll
+      for (int j = 0; j < S; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + j * SRC + lane * LCB);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const I4Fma k = i4_fma_scale(sc[j]);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          if (j == 0) dequant_set_i4(w[m], k, acc[m]);
+          else dequant_acc_i4(w[m], k, one2, acc[m]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[m][i] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < S; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + j * SRC + lane * LCB);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        lane32_dequant_acc<BITS>(w, sc[j], false, a.one, acc);
+      }
+    }
+    // requantize the lane's 32 sums with its block's scale
+    const Scale sco = lane32_block_scale<QMAX, LOGB, WPB>(acc, red, parity, warp, gid, lane);
+    const int64_t e_warp = t * G::U + (int64_t)wsub * G::kWarpElems;
+    const int64_t obase = ((int64_t)dn * a.G + dl) * a.R + e_warp;
+    lane32_quantize_store<BITS>(acc, sco, a.codes_out + ((obase * BITS) >> 3) + lane * LCB);
+    const int eb = (int)(e_warp & (G::B - 1)) + lane_e;
+    if ((eb & (G::B - 1)) == 0) a.scales_out[(obase >> LOGB) + (eb >> LOGB)] = sco.s;
+    __syncwarp();  // every lane has read its scales before the stage is refilled
+    next_unit(t, dn, dl);
+    next_unit(t1, dn1, dl1);
+  }
+  cp_async_wait<0>();  // no copy outlives the warp
+}
+
 template <int BITS, int MODE>
 cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
   return dispatch_logb(block, [&](auto lb) -> cudaError_t {
@@ -557,6 +725,17 @@ cudaError_t run_hop(const HopArgs& a0, int block, cudaStream_t st) {
           const void* k = reinterpret_cast<const void*>(&hop1_kernel<BITS, LOGB, S>);
           hop1_kernel<BITS, LOGB, S><<<grid_for(k, ctas), kThreads, 0, st>>>(a);
         };
+        if constexpr (BITS == 4) {
+          if (a.S == kStagedSources) {
+            constexpr size_t smem = (size_t)kWarps * 2 * hop1_stage_bytes<LOGB>();
+            const void* k = reinterpret_cast<const void*>(&hop1_staged_kernel<LOGB>);
+            const cudaError_t e = smem_opt_in(k, smem);
+            if (e != cudaSuccess) return e;
+            hop1_staged_kernel<LOGB>
+                <<<grid_for(k, ctas, smem, kHop1StagedRounds), kThreads, smem, st>>>(a);
+            return cudaGetLastError();
+          }
+        }
         if (BITS == 4 && a.S % 8 == 0) launch1(std::integral_constant<int, BITS == 4 ? 4 : 2>{});
         else launch1(std::integral_constant<int, 2>{});
         return cudaGetLastError();

@@ -180,7 +180,7 @@ def hop1_input(N, G, block, bits, L, rng):
 
 
 @pytest.mark.parametrize("bits", [4, 8])
-@pytest.mark.parametrize("block", [64, 256, 512, 2048])
+@pytest.mark.parametrize("block", [64, 128, 256, 512, 1024, 2048, 4096])
 @pytest.mark.parametrize("N,G", [(2, 4), (2, 8), (3, 8)])
 def test_hop1_whole_unit_slices(bits, block, N, G):
     """Hop 1 where every destination row is whole 1024-element warp units and
@@ -191,6 +191,35 @@ def test_hop1_whole_unit_slices(bits, block, N, G):
     c2, s2 = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
     nl = N * L
     Nd = N * G
+    out_c = torch.full((Nd * Z.zpp_codes_bytes(nl, bits),), 0x5A, dtype=torch.uint8, device="cuda")
+    out_s = torch.full((Nd * (nl // block),), float("nan"), device="cuda")
+    Z.zpp_qgz_hop_reduce(1, torch.from_numpy(c1).cuda(), torch.from_numpy(s1).cuda(), N, G,
+                         bucket, block, bits, codes_out=out_c, scales_out=out_s)
+    torch.cuda.synchronize()
+    assert_bytes_equal(np_bytes(out_c), c2, "hop-1 codes")
+    assert_f32_bitexact(np_f32(out_s), s2, "hop-1 scales")
+
+
+@pytest.mark.parametrize("block", [128, 512, 2048])
+def test_hop1_several_units_a_warp(block):
+    """Int4 hop 1 with eight sources on a bucket large enough that warp groups
+    get more than one unit each (the grid is capped at a few rounds of resident
+    CTAs), so stages are refilled and, for B = 2048, the two-slot cross-warp
+    absmax alternates; random one-shot messages with scales above 2^-5, zero and
+    subnormal scales mixed in, against the oracle."""
+    Z = zpp()
+    N, G, bits = 2, 8, 4
+    Nd = N * G
+    L = 1 << 19
+    bucket = Nd * L
+    rng = np.random.default_rng(block)
+    c1 = rng.integers(0, 256, size=Nd * bucket // 2, dtype=np.uint8)
+    s1 = (rng.random(Nd * bucket // block, dtype=np.float32) * 1e-3).astype(np.float32)
+    s1[::29] *= 100.0                                  # above 2^-5
+    s1[3::31] = 0.0
+    s1[7::37] = rng.integers(1, 5000, size=s1[7::37].shape) * np.float32(2.0 ** -149)
+    c2, s2 = oracle.qgz_hop1(c1, s1, N, G, bucket, block, bits)
+    nl = N * L
     out_c = torch.full((Nd * Z.zpp_codes_bytes(nl, bits),), 0x5A, dtype=torch.uint8, device="cuda")
     out_s = torch.full((Nd * (nl // block),), float("nan"), device="cuda")
     Z.zpp_qgz_hop_reduce(1, torch.from_numpy(c1).cuda(), torch.from_numpy(s1).cuda(), N, G,
