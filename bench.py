@@ -57,6 +57,23 @@ KERNEL_OF = {  # launch name -> CUDA kernel (for the roofline and the ncu summar
     "ring_step": "ring1_kernel<BITS, LOGB, MODE, WIDE>",
     "ring_adam": "adam_kernel<WIDE>",
 }
+
+
+def kernel_label(name, wl):
+    """The CUDA kernel a launch runs on this workload: hop 1 picks its kernel by
+    width, sources per node and whether every destination row is whole warp units,
+    as the library's launcher does."""
+    g = wl.qgz
+    if name != "qgz_hop1" or g is None:
+        return KERNEL_OF[name]
+    whole = (g.nodes * (g.bucket // g.nd)) % max(1024, g.block) == 0
+    if whole and g.gpus_per_node % 4 == 0:
+        return ("hop1_staged_kernel<LOGB>" if g.bits == 4 and g.gpus_per_node == 8
+                else "hop1_kernel<BITS, LOGB, SCH>")
+    return ("hop_tiled_kernel<BITS, kRequant, LOGB, false, SCH>" if whole
+            else "hop_kernel<BITS, kRequant, LOGB>")
+
+
 KERNEL_SRC = {"qwz_quant": "quant.cu", "qwz_dequant": "quant.cu", "qgz_reorder_quant": "quant.cu",
               "qgz_hop1": "hop.cu", "qgz_final_hop": "hop.cu", "qgz_final_hop_qwz": "hop.cu",
               "grad_accumulate": "quant.cu", "qgz_reorder_quant_acc": "quant.cu",
@@ -417,7 +434,7 @@ def run_gpu(args, wl, rank, world, device):
     for name, ts in per.items():
         nb = sum(bytes_of[name]) / len(bytes_of[name])
         avg = sum(ts) / len(ts)
-        kernels[name] = {"kernel": KERNEL_OF[name], "launches": len(ts), "avg_ms": avg,
+        kernels[name] = {"kernel": kernel_label(name, wl), "launches": len(ts), "avg_ms": avg,
                          "bytes_per_launch": nb, "gbs": nb / (avg * 1e-3) / 1e9,
                          "frac_of_peak": nb / (avg * 1e-3) / 1e9 / peak,
                          "share": sum(ts) / total_ms}
