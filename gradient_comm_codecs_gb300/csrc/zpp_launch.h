@@ -84,9 +84,10 @@ int grid_for(const void* kernel, int64_t work_ctas, size_t smem = 0, int waves =
 // of the copy peak, the dequantizer 0.91 -> 0.99, the reorder quantizer
 // 0.94 -> 1.00 and Adam 0.97 -> 0.99; from 24 rounds on the quantizers lose
 // again (a warp group then gets one or two units, and each CTA's start-up --
-// its first copies in flight -- is no longer amortised).  The hop kernels
-// (two CTAs an SM, heavy per-CTA set-up) stay persistent: no round count
-// changed them.
+// its first copies in flight -- is no longer amortised).  The register-chunk
+// hop kernels (two CTAs an SM, heavy per-CTA set-up) stay persistent: no round
+// count changed them.  The staged int4 hop 1 and the ring step pick their own
+// round counts (four each).
 constexpr int kStreamWaves = 8;
 
 // Raises the kernel's dynamic shared-memory limit to `smem` bytes on the
