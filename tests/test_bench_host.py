@@ -1,7 +1,7 @@
 """Host logic of bench.py that needs no GPU: the clock summary taken from
 nvidia-smi samples during the timed region (median SM clock, the throttle
 reasons seen, the fallback window for a region shorter than the sampling
-period, unreadable fields)."""
+period, unreadable fields), and the kernel name a launch is reported under."""
 import bench
 
 
@@ -45,3 +45,26 @@ def test_unreadable_fields_are_skipped():
 def test_no_samples():
     s = sampler_with([]).summary(0.0, 1.0)
     assert s["sm_mhz"] is None and s["samples"] == 0 and s["reasons"] == []
+
+
+def test_hop1_kernel_label_follows_the_launcher():
+    """The bench names the kernel hop 1 runs on a workload by the launcher's
+    rules: int4 with eight sources a node on whole warp units takes the staged
+    kernel, other widths and source counts that are multiples of four the
+    register-chunk kernel, other whole-unit rows the tiled hop kernel and
+    ragged rows the general one."""
+    import dataclasses
+    from synth import workloads as W
+    assert bench.kernel_label("qgz_hop1", W.WORKLOADS["7b"]) == "hop1_staged_kernel<LOGB>"
+    assert bench.kernel_label("qgz_hop1", W.WORKLOADS["two_hop"]) == "hop1_staged_kernel<LOGB>"
+    wl = W.WORKLOADS["two_hop"]
+    g = wl.qgz
+    int8 = dataclasses.replace(wl, qgz=dataclasses.replace(g, bits=8))
+    assert bench.kernel_label("qgz_hop1", int8) == "hop1_kernel<BITS, LOGB, SCH>"
+    g4 = dataclasses.replace(wl, qgz=dataclasses.replace(g, gpus_per_node=4))
+    assert bench.kernel_label("qgz_hop1", g4) == "hop1_kernel<BITS, LOGB, SCH>"
+    assert bench.kernel_label("qgz_hop1", W.WORKLOADS["tiny"]).startswith("hop_tiled_kernel")
+    # 2 x 8 ranks with 3 * 256-element slices: rows of 1536 elements, not whole 1024-element units
+    ragged = dataclasses.replace(wl, qgz=dataclasses.replace(g, bucket=16 * 3 * 256))
+    assert bench.kernel_label("qgz_hop1", ragged).startswith("hop_kernel")
+    assert bench.kernel_label("qwz_quant", wl) == bench.KERNEL_OF["qwz_quant"]
