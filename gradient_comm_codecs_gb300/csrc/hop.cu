@@ -546,10 +546,11 @@ __global__ void __launch_bounds__(kThreads, 2) hop1_kernel(const HopArgs a) {
 // With no code registers held across units the kernel needs 80 registers, so
 // three CTAs (24 warps) fit an SM next to their 3 x 66 KB of stages, and
 // cp.async.wait_group is a hardware wait: on GB300 the long-scoreboard stalls
-// per issue fall from 1.19 to 0.25 against hop1_kernel and issue goes from 62%
-// to 68% active, for 2% more instructions (the copies and the shared-memory
-// reads); what is left is the decode's ALU work.  The first source of a unit
-// is written straight into the accumulator (dequant_set_i4).
+// per issue fall from about 1.2 to 0.07-0.25 against hop1_kernel and issue
+// goes from 62-64% to 68-72% active, for 5% more instructions (the copies, the
+// shared-memory reads and the start-up of four times as many CTAs); what is
+// left is the decode's ALU work.  The first source of a unit is written
+// straight into the accumulator (dequant_set_i4).
 // acc[i] = RN(q_i s), i = 0..7: the first source of a sum written straight
 // into the accumulator instead of added to a zero one.  The two differ only
 // where RN(q s) is -0 (0 + -0 is +0), and a requantizing sum cannot tell: the
