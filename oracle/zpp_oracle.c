@@ -7,6 +7,13 @@
  * tests, the entry point's smoke check and the bench's CPU-baseline leg do.
  * It shares no code, header, table or helper with the CUDA library.
  *
+ * Pins: each function here is checked by the test suite against something
+ * other than itself (brute force, closed forms, exact sums, the pages'
+ * numbers).  The two-hop chain with a real int4/int8 codec is parity
+ * unpinned beyond an error bound: its pieces (the block codec, the summation
+ * order, the slice placement) are pinned one by one, and the composed values
+ * only by the sum of the half-scales they went through.
+ *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fno-fast-math -fPIC -shared.
  * Every floating-point operation below is a separately rounded IEEE fp32
  * operation (no FMA contraction), in the order written.
